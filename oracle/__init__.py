@@ -1,0 +1,174 @@
+"""CPU oracle for the collective reduction math.  TEST INFRASTRUCTURE ONLY.
+
+Only the test suite, ``__graft_entry__.smoke()`` and the CPU-baseline leg of
+``bench.py`` may import this package.  The CUDA library never imports it, and
+the two share no code: the oracle is plain single-threaded C (``oracle.c``)
+compiled with gcc and reached through ctypes.
+
+Buffers are numpy arrays: fp32 as ``float32``, bf16 as ``uint16`` bit
+patterns, int32 as ``int32``.
+
+What each routine follows (page title and section):
+  * ``allreduce`` / ``reduce_scatter`` / ``all_gather``: "What all-reduce
+    promises" and "The ring, exactly as the kernel runs it" (post on NCCL
+    all-reduce); "All-gather: everyone shows their piece" and "Why backward
+    needs a different collective" (FSDP collectives 101).
+  * ``ring_order``: "The ring, exactly as the kernel runs it".
+  * ``tree``: "The double binary tree".
+  * ``chunk_lo``: Eq. (2), "Local shard bounds" (NCCL M2N).
+  * ``bf16_rne``: the single bf16 rounding of an fp32 accumulator.
+
+Parity unpinned: NaN and infinity payloads through min/max and bf16 rounding.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "oracle.c")
+_LIB_PATH = os.path.join(_HERE, "liboracle.so")
+
+DTYPES = {"fp32": 0, "bf16": 1, "int32": 2}
+OPS = {"sum": 0, "prod": 1, "min": 2, "max": 3, "avg": 4}
+ALGOS = {"ring": 0, "tree": 1}
+NP_DTYPE = {"fp32": np.float32, "bf16": np.uint16, "int32": np.int32}
+
+_lib = None
+
+
+def build(force: bool = False) -> str:
+    """Compile oracle.c into liboracle.so with gcc (no FMA contraction)."""
+    if (not force and os.path.exists(_LIB_PATH)
+            and os.path.getmtime(_LIB_PATH) >= max(os.path.getmtime(_SRC),
+                                                  os.path.getmtime(os.path.join(_HERE, "oracle.h")))):
+        return _LIB_PATH
+    tmp = _LIB_PATH + f".tmp{os.getpid()}"
+    cmd = ["gcc", "-O2", "-std=c11", "-ffp-contract=off", "-fno-fast-math",
+           "-fPIC", "-shared", "-Wall", "-Wextra", "-o", tmp, _SRC, "-lm"]
+    subprocess.run(cmd, check=True)
+    os.replace(tmp, _LIB_PATH)
+    return _LIB_PATH
+
+
+def lib():
+    global _lib
+    if _lib is None:
+        build()
+        L = ctypes.CDLL(_LIB_PATH)
+        vp, sz, i = ctypes.c_void_p, ctypes.c_size_t, ctypes.c_int
+        L.or_f32_to_bf16_rne.argtypes = [ctypes.c_float]
+        L.or_f32_to_bf16_rne.restype = ctypes.c_uint16
+        L.or_f32_to_bf16_rne_array.argtypes = [vp, vp, sz]
+        L.or_f32_to_bf16_rne_array.restype = None
+        L.or_chunk_lo.argtypes = [i, sz, i]
+        L.or_chunk_lo.restype = sz
+        L.or_ring_order.argtypes = [i, i, vp]
+        L.or_ring_order.restype = None
+        L.or_tree_build.argtypes = [i, i, vp, vp]
+        L.or_tree_build.restype = i
+        L.or_allreduce.argtypes = [i, i, i, i, sz, vp, vp]
+        L.or_allreduce.restype = i
+        L.or_reduce_scatter.argtypes = [i, i, i, i, sz, vp, vp]
+        L.or_reduce_scatter.restype = i
+        L.or_all_gather.argtypes = [i, i, sz, vp, vp]
+        L.or_all_gather.restype = i
+        L.or_reduce_one.argtypes = [i, i, i, i, sz, sz, vp, vp]
+        L.or_reduce_one.restype = i
+        _lib = L
+    return _lib
+
+
+def _ptrs(arrays):
+    arr = (ctypes.c_void_p * len(arrays))(*[a.ctypes.data for a in arrays])
+    return arr
+
+
+def _check_inputs(dtype, arrays, n):
+    want = NP_DTYPE[dtype]
+    for a in arrays:
+        if a.dtype != want or not a.flags.c_contiguous or a.size != n:
+            raise ValueError(f"oracle input must be contiguous {want.__name__}[{n}]")
+
+
+def allreduce(dtype: str, op: str, algo: str, inputs, all_ranks: bool = False):
+    """All-reduce of W rank buffers.  Returns one copy of the (identical)
+    result, or with ``all_ranks`` the list of every rank's output buffer."""
+    W, N = len(inputs), inputs[0].size
+    _check_inputs(dtype, inputs, N)
+    copies = W if all_ranks else 1
+    outs = [np.empty(N, NP_DTYPE[dtype]) for _ in range(copies)]
+    out_ptrs = [outs[j % copies] for j in range(W)]
+    rc = lib().or_allreduce(DTYPES[dtype], OPS[op], ALGOS[algo], W, N, _ptrs(inputs), _ptrs(out_ptrs))
+    if rc != 0:
+        raise ValueError("oracle allreduce rejected its arguments")
+    return outs if all_ranks else outs[0]
+
+
+def reduce_scatter(dtype: str, op: str, algo: str, inputs):
+    """Reduce-scatter: returns W shards; shard k is chunk k of the result."""
+    W, N = len(inputs), inputs[0].size
+    _check_inputs(dtype, inputs, N)
+    if N % W:
+        raise ValueError("reduce-scatter needs N divisible by W")
+    outs = [np.empty(N // W, NP_DTYPE[dtype]) for _ in range(W)]
+    rc = lib().or_reduce_scatter(DTYPES[dtype], OPS[op], ALGOS[algo], W, N, _ptrs(inputs), _ptrs(outs))
+    if rc != 0:
+        raise ValueError("oracle reduce_scatter rejected its arguments")
+    return outs
+
+
+def all_gather(dtype: str, shards, all_ranks: bool = False):
+    """All-gather of W shards: one copy of the full buffer, or every rank's."""
+    W, C = len(shards), shards[0].size
+    _check_inputs(dtype, shards, C)
+    copies = W if all_ranks else 1
+    outs = [np.empty(C * W, NP_DTYPE[dtype]) for _ in range(copies)]
+    out_ptrs = [outs[j % copies] for j in range(W)]
+    rc = lib().or_all_gather(DTYPES[dtype], W, C * W, _ptrs(shards), _ptrs(out_ptrs))
+    if rc != 0:
+        raise ValueError("oracle all_gather rejected its arguments")
+    return outs if all_ranks else outs[0]
+
+
+def reduce_one(dtype: str, op: str, algo: str, N: int, e: int, y):
+    """Result at element e of an N-element all-reduce, from the W values y[r]."""
+    y = np.ascontiguousarray(y, dtype=NP_DTYPE[dtype])
+    res = np.empty(1, NP_DTYPE[dtype])
+    rc = lib().or_reduce_one(DTYPES[dtype], OPS[op], ALGOS[algo], y.size, N, e,
+                             y.ctypes.data, res.ctypes.data)
+    if rc != 0:
+        raise ValueError("oracle reduce_one rejected its arguments")
+    return res[0]
+
+
+def ring_order(W: int, k: int):
+    out = np.empty(W, np.int32)
+    lib().or_ring_order(W, k, out.ctypes.data)
+    return out.tolist()
+
+
+def tree(W: int, which: int):
+    """Returns (root, parent[W], children[W] as lists)."""
+    parent = np.empty(W, np.int32)
+    child = np.empty(2 * W, np.int32)
+    root = lib().or_tree_build(W, which, parent.ctypes.data, child.ctypes.data)
+    if root < 0:
+        raise ValueError("bad W")
+    kids = [[c for c in child[2 * r:2 * r + 2].tolist() if c >= 0] for r in range(W)]
+    return root, parent.tolist(), kids
+
+
+def chunk_lo(W: int, N: int, k: int) -> int:
+    return int(lib().or_chunk_lo(W, N, k))
+
+
+def bf16_rne(bits_u32) -> np.ndarray:
+    """Round fp32 bit patterns (uint32 array) to bf16 patterns (uint16)."""
+    a = np.ascontiguousarray(bits_u32, dtype=np.uint32)
+    out = np.empty(a.size, np.uint16)
+    lib().or_f32_to_bf16_rne_array(a.ctypes.data, out.ctypes.data, a.size)
+    return out

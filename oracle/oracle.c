@@ -1,0 +1,340 @@
+/*
+ * oracle.c -- the CPU oracle.  TEST INFRASTRUCTURE ONLY (see oracle.h).
+ *
+ * Compiled with -ffp-contract=off so that no multiply-add is ever fused: every
+ * fp32 operation below is one IEEE binary32 operation, rounded to nearest even.
+ * Single-threaded, element by element, in the order the method defines.
+ */
+#include "oracle.h"
+
+#include <math.h>
+#include <string.h>
+
+/* ------------------------------------------------------------------------- */
+/* Element access                                                            */
+/* ------------------------------------------------------------------------- */
+
+typedef union {
+    float f;     /* fp32 and bf16 accumulate in fp32 */
+    uint32_t u;  /* int32 accumulates in 32-bit two's complement, wrapping */
+} acc_t;
+
+static size_t elem_size(int dtype) { return dtype == OR_BF16 ? 2u : 4u; }
+
+/*
+ * bf16 -> fp32 is exact: the bf16 pattern is the top half of the fp32 pattern.
+ * int32 is kept as its bit pattern so that sum and product wrap modulo 2^32.
+ */
+static acc_t widen(int dtype, const void* buf, size_t e) {
+    acc_t a;
+    if (dtype == OR_BF16) {
+        uint16_t h;
+        memcpy(&h, (const char*)buf + 2u * e, 2);
+        a.u = (uint32_t)h << 16;
+    } else {
+        memcpy(&a.u, (const char*)buf + 4u * e, 4);
+    }
+    return a;
+}
+
+/* ------------------------------------------------------------------------- */
+/* bf16 rounding                                                             */
+/* ------------------------------------------------------------------------- */
+
+/*
+ * Nearest bf16, ties to even.  Adding 0x7FFF plus the lowest kept bit to the
+ * fp32 pattern carries into the kept half exactly when the dropped half is
+ * above one half, or exactly one half with an odd kept half.  Values past the
+ * largest finite bf16 carry into the exponent and become +-infinity.  A NaN
+ * keeps its sign and is made quiet.
+ */
+uint16_t or_f32_to_bf16_rne(float x) {
+    uint32_t u;
+    memcpy(&u, &x, 4);
+    if ((u & 0x7F800000u) == 0x7F800000u && (u & 0x007FFFFFu) != 0u)
+        return (uint16_t)((u >> 16) | 0x0040u);
+    u += 0x7FFFu + ((u >> 16) & 1u);
+    return (uint16_t)(u >> 16);
+}
+
+void or_f32_to_bf16_rne_array(const uint32_t* in, uint16_t* out, size_t n) {
+    for (size_t i = 0; i < n; i++) {
+        float f;
+        memcpy(&f, &in[i], 4);
+        out[i] = or_f32_to_bf16_rne(f);
+    }
+}
+
+/* ------------------------------------------------------------------------- */
+/* The reduction ops ("What all-reduce promises": sum, prod, min, max, avg)  */
+/* ------------------------------------------------------------------------- */
+
+/* min and max order -0 below +0, so that both are independent of the order
+ * in which the ranks are visited. */
+static float min_f32(float a, float b) {
+    if (b < a) return b;
+    if (a < b) return a;
+    if (a == 0.0f && b == 0.0f) return signbit(b) ? b : a;
+    return a;
+}
+
+static float max_f32(float a, float b) {
+    if (a < b) return b;
+    if (b < a) return a;
+    if (a == 0.0f && b == 0.0f) return signbit(b) ? a : b;
+    return a;
+}
+
+/* a (+) b for the op; avg combines like sum. */
+static acc_t combine(int dtype, int op, acc_t a, acc_t b) {
+    if (dtype == OR_INT32) {
+        switch (op) {
+        case OR_SUM:
+        case OR_AVG: a.u = a.u + b.u; break;
+        case OR_PROD: a.u = a.u * b.u; break;
+        case OR_MIN: if ((int32_t)b.u < (int32_t)a.u) a = b; break;
+        case OR_MAX: if ((int32_t)a.u < (int32_t)b.u) a = b; break;
+        }
+    } else {
+        switch (op) {
+        case OR_SUM:
+        case OR_AVG: a.f = a.f + b.f; break;
+        case OR_PROD: a.f = a.f * b.f; break;
+        case OR_MIN: a.f = min_f32(a.f, b.f); break;
+        case OR_MAX: a.f = max_f32(a.f, b.f); break;
+        }
+    }
+    return a;
+}
+
+/*
+ * The pre-scale of a float avg: each contribution is multiplied by 1/W as it
+ * is read, with 1/W rounded once to fp32.  Integers are not scaled.
+ */
+static float avg_scale(int W) { return (float)(1.0 / (double)W); }
+
+static acc_t read_contribution(int dtype, int op, float s, const void* buf, size_t e) {
+    acc_t y = widen(dtype, buf, e);
+    if (op == OR_AVG && dtype != OR_INT32) y.f = y.f * s;
+    return y;
+}
+
+/* The postOp at the step where a chunk's sum completes: one truncating divide
+ * of the finished integer sum for avg, one bf16 rounding for bf16, nothing for
+ * fp32.  Writes element e of buf. */
+static void store_result(int dtype, int op, int W, acc_t acc, void* buf, size_t e) {
+    if (dtype == OR_FP32) {
+        memcpy((char*)buf + 4u * e, &acc.u, 4);
+    } else if (dtype == OR_BF16) {
+        uint16_t h = or_f32_to_bf16_rne(acc.f);
+        memcpy((char*)buf + 2u * e, &h, 2);
+    } else {
+        int32_t v = (int32_t)acc.u;
+        if (op == OR_AVG) v = v / W;
+        memcpy((char*)buf + 4u * e, &v, 4);
+    }
+}
+
+/* ------------------------------------------------------------------------- */
+/* Chunking (Eq. 2 of the M2N paper: l = floor(i*S/D))                       */
+/* ------------------------------------------------------------------------- */
+
+size_t or_chunk_lo(int W, size_t N, int k) {
+    /* floor(k*N/W) without forming k*N: N = q*W + r. */
+    size_t q = N / (size_t)W, r = N % (size_t)W;
+    return (size_t)k * q + ((size_t)k * r) / (size_t)W;
+}
+
+/* ------------------------------------------------------------------------- */
+/* Ring order ("The ring, exactly as the kernel runs it")                    */
+/* ------------------------------------------------------------------------- */
+
+/*
+ * With ranks in a ring 0 -> 1 -> ... -> W-1 -> 0, rank k+1 sends its own part
+ * of chunk k first; each of the next W-1 hops adds the receiving rank's part;
+ * the total is complete on rank k, which owns chunk k.
+ */
+void or_ring_order(int W, int k, int* order) {
+    for (int i = 0; i < W; i++) order[i] = (k + 1 + i) % W;
+}
+
+/* ------------------------------------------------------------------------- */
+/* Double binary tree ("The double binary tree")                             */
+/* ------------------------------------------------------------------------- */
+
+/*
+ * Tree 1: the lowest set bit b of rank r fixes its depth (rank 0, the root,
+ * takes b = the smallest power of two >= W).  Parent: clear b and set the next
+ * bit up; if that falls outside the ranks, just clear b.  Children: r - b/2
+ * (for b > 1), and r + h for the largest h in b/2, b/4, ..., 1 that stays
+ * inside the ranks.
+ */
+static void tree1(int W, int* parent, int* child) {
+    int B = 1;
+    while (B < W) B <<= 1;
+    for (int r = 0; r < W; r++) {
+        int b = (r == 0) ? B : (r & -r);
+        if (r == 0) {
+            parent[r] = -1;
+        } else {
+            int p = (r & ~b) | (b << 1);
+            if (p >= W) p = r & ~b;
+            parent[r] = p;
+        }
+        int n = 0;
+        child[2 * r] = child[2 * r + 1] = -1;
+        if (r > 0 && b > 1) child[2 * r + n++] = r - b / 2;
+        for (int h = b / 2; h >= 1; h /= 2) {
+            if (r + h < W) {
+                child[2 * r + n++] = r + h;
+                break;
+            }
+        }
+    }
+}
+
+/*
+ * Tree 2 swaps the roles of leaves and interior ranks: for even W it is the
+ * mirror image of tree 1 (rank W-1-r takes the place of r); for odd W it is
+ * tree 1 shifted by one rank (rank (r+1) mod W takes the place of r).
+ */
+static int tree2_rank(int W, int r) { return (W % 2 == 0) ? (W - 1 - r) : ((r + 1) % W); }
+
+int or_tree_build(int W, int which, int* parent, int* child) {
+    int p1[OR_MAX_RANKS], c1[2 * OR_MAX_RANKS];
+    if (W < 1 || W > OR_MAX_RANKS) return -1;
+    tree1(W, p1, c1);
+    if (which == 1) {
+        memcpy(parent, p1, sizeof(int) * (size_t)W);
+        memcpy(child, c1, sizeof(int) * 2u * (size_t)W);
+        return 0;
+    }
+    for (int r = 0; r < W; r++) {
+        int m = tree2_rank(W, r);
+        parent[m] = p1[r] < 0 ? -1 : tree2_rank(W, p1[r]);
+        for (int i = 0; i < 2; i++)
+            child[2 * m + i] = c1[2 * r + i] < 0 ? -1 : tree2_rank(W, c1[2 * r + i]);
+    }
+    return tree2_rank(W, 0);
+}
+
+/* Reduce up the tree, each parent adding its children's subtotals to its own
+ * contribution: subtotal(v) = y_v (+) subtotal(first child) (+) subtotal(second). */
+static acc_t tree_subtotal(int dtype, int op, int v, const int* child, const acc_t* y) {
+    acc_t acc = y[v];
+    for (int i = 0; i < 2; i++) {
+        int c = child[2 * v + i];
+        if (c >= 0) acc = combine(dtype, op, acc, tree_subtotal(dtype, op, c, child, y));
+    }
+    return acc;
+}
+
+/* ------------------------------------------------------------------------- */
+/* The reduction of one element position                                     */
+/* ------------------------------------------------------------------------- */
+
+typedef struct {
+    int dtype, op, algo, W;
+    size_t N;
+    float s;
+    int root[2];
+    int child[2][2 * OR_MAX_RANKS];
+} plan_t;
+
+static int make_plan(plan_t* P, int dtype, int op, int algo, int W, size_t N) {
+    int parent[OR_MAX_RANKS];
+    if (W < 1 || W > OR_MAX_RANKS) return -1;
+    if (dtype < OR_FP32 || dtype > OR_INT32) return -1;
+    if (op < OR_SUM || op > OR_AVG) return -1;
+    if (algo != OR_RING && algo != OR_TREE) return -1;
+    P->dtype = dtype;
+    P->op = op;
+    P->algo = algo;
+    P->W = W;
+    P->N = N;
+    P->s = avg_scale(W);
+    P->root[0] = or_tree_build(W, 1, parent, P->child[0]);
+    P->root[1] = or_tree_build(W, 2, parent, P->child[1]);
+    return 0;
+}
+
+/* y[r] = rank r's (pre-scaled) contribution at element e, which lies in chunk k. */
+static acc_t reduce_position(const plan_t* P, int k, size_t e, const acc_t* y) {
+    if (P->algo == OR_RING) {
+        int order[OR_MAX_RANKS];
+        or_ring_order(P->W, k, order);
+        acc_t acc = y[order[0]];
+        for (int i = 1; i < P->W; i++) acc = combine(P->dtype, P->op, acc, y[order[i]]);
+        return acc;
+    }
+    /* The first floor(N/2) elements climb tree 1, the rest tree 2. */
+    int t = (e < P->N / 2) ? 0 : 1;
+    return tree_subtotal(P->dtype, P->op, P->root[t], P->child[t], y);
+}
+
+static acc_t reduce_from_buffers(const plan_t* P, int k, size_t e, const void* const* in) {
+    acc_t y[OR_MAX_RANKS];
+    for (int r = 0; r < P->W; r++) y[r] = read_contribution(P->dtype, P->op, P->s, in[r], e);
+    return reduce_position(P, k, e, y);
+}
+
+/* ------------------------------------------------------------------------- */
+/* The collectives                                                           */
+/* ------------------------------------------------------------------------- */
+
+int or_allreduce(int dtype, int op, int algo, int W, size_t N,
+                 const void* const* in, void* const* out) {
+    plan_t P;
+    if (make_plan(&P, dtype, op, algo, W, N) != 0) return -1;
+    for (int k = 0; k < W; k++) {
+        size_t lo = or_chunk_lo(W, N, k), hi = or_chunk_lo(W, N, k + 1);
+        for (size_t e = lo; e < hi; e++) {
+            acc_t acc = reduce_from_buffers(&P, k, e, in);
+            for (int j = 0; j < W; j++) store_result(dtype, op, W, acc, out[j], e);
+        }
+    }
+    return 0;
+}
+
+int or_reduce_scatter(int dtype, int op, int algo, int W, size_t N,
+                      const void* const* in, void* const* out) {
+    plan_t P;
+    if (make_plan(&P, dtype, op, algo, W, N) != 0) return -1;
+    if (N % (size_t)W != 0) return -1;
+    for (int k = 0; k < W; k++) {
+        size_t lo = or_chunk_lo(W, N, k), hi = or_chunk_lo(W, N, k + 1);
+        for (size_t e = lo; e < hi; e++) {
+            acc_t acc = reduce_from_buffers(&P, k, e, in);
+            store_result(dtype, op, W, acc, out[k], e - lo);
+        }
+    }
+    return 0;
+}
+
+int or_all_gather(int dtype, int W, size_t N, const void* const* in, void* const* out) {
+    if (W < 1 || W > OR_MAX_RANKS) return -1;
+    if (dtype < OR_FP32 || dtype > OR_INT32) return -1;
+    if (N % (size_t)W != 0) return -1;
+    size_t b = elem_size(dtype);
+    for (int k = 0; k < W; k++) {
+        size_t lo = or_chunk_lo(W, N, k), hi = or_chunk_lo(W, N, k + 1);
+        for (size_t i = 0; i < hi - lo; i++)
+            for (int j = 0; j < W; j++)
+                memcpy((char*)out[j] + b * (lo + i), (const char*)in[k] + b * i, b);
+    }
+    return 0;
+}
+
+int or_reduce_one(int dtype, int op, int algo, int W, size_t N, size_t e,
+                  const void* y_raw, void* res) {
+    plan_t P;
+    acc_t y[OR_MAX_RANKS];
+    if (make_plan(&P, dtype, op, algo, W, N) != 0) return -1;
+    if (e >= N) return -1;
+    int k = 0;
+    while (or_chunk_lo(W, N, k + 1) <= e) k++;
+    for (int r = 0; r < W; r++) y[r] = read_contribution(dtype, op, P.s, y_raw, (size_t)r);
+    acc_t acc = reduce_position(&P, k, e, y);
+    store_result(dtype, op, W, acc, res, 0);
+    return 0;
+}
