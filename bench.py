@@ -1,0 +1,469 @@
+#!/usr/bin/env python3
+"""Fused all-reduce algo GB/s and fraction of the HBM roofline on one GB300.
+
+One step = one fused ring all-reduce (avg) of the DDP gradient-bucket workload:
+W = 8 simulated ranks, 2^24 fp32 per rank (64 MiB), Normal(0, 1e-3), through
+the C ABI (mr_allreduce).  Algorithmic bytes per step: 2*W*N*4 = 1 GiB (W
+reads and W writes of N elements).  Inputs are resident in HBM before the
+timed region and larger than L2, so no flush is needed between steps.
+
+Prints ONE JSON line (rank 0).  With --gpus N under torchrun every rank runs
+an independent replica on its own GPU (the simulated ranks never cross GPUs):
+value = all replicas' bytes / the slowest rank's time.
+
+--impl reference times the CPU oracle on the host cores instead (a bounded
+sample of the same workload per step).
+"""
+from __future__ import annotations
+
+import argparse
+import datetime
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "fused all-reduce algo GB/s and % of GB300 HBM roofline vs message size"
+WORKLOAD = "ddp_bucket_fp32_w8"
+FALLBACK_HBM_GBS = 6800.0
+L2_BYTES = 129 * 1000 * 1000
+KERNEL_SOURCES = ["reduce_kernel.cuh", "order.cuh", "mr_internal.h", "reduce_fp32.cu", "api.cu"]
+PROFILE = os.path.join(ROOT, "profiles", "reduce_kernel_ddp_bucket_fp32_w8.txt")
+
+
+def parse_args():
+    p = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=8000)
+    p.add_argument("--warmup", type=int, default=20)
+    p.add_argument("--impl", choices=["mine", "reference"], default="mine")
+    p.add_argument("--no-extras", action="store_true", help="skip the size sweep and the other workloads")
+    p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--e2e-steps", type=int, default=20)
+    return p.parse_args()
+
+
+def cpu_model() -> str:
+    try:
+        with open("/proc/cpuinfo") as f:
+            for line in f:
+                if line.lower().startswith(("model name", "cpu part", "hardware")):
+                    return line.split(":", 1)[1].strip()
+    except OSError:
+        pass
+    return "unknown"
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "MEASURED_PEAKS.json hbm_gbs (burst copy), of measured"
+    except (OSError, KeyError, ValueError):
+        return FALLBACK_HBM_GBS, "6.8 TB/s recipe figure, of fallback"
+
+
+def kernel_source_hash() -> str:
+    h = hashlib.sha256()
+    for fn in KERNEL_SOURCES:
+        with open(os.path.join(ROOT, "collective_reduction_math_gb300", "csrc", fn), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()
+
+
+def profiled_traffic():
+    """DRAM bytes per launch from the committed ncu summary, if it was taken on
+    the kernel sources as they are now; else None."""
+    try:
+        kv = {}
+        with open(PROFILE) as f:
+            for line in f:
+                if ":" in line and not line.startswith("#"):
+                    k, v = line.split(":", 1)
+                    kv[k.strip()] = v.strip()
+        if kv.get("kernel_source_sha256") != kernel_source_hash():
+            return None
+        return int(float(kv["traffic_bytes_per_launch"]))
+    except (OSError, KeyError, ValueError):
+        return None
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled every 100 ms."""
+
+    FIELDS = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu_index = gpu_index
+        self.proc = None
+        self.out = None
+        self.t0 = self.t1 = None
+
+    def start(self):
+        self.out = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=self.out, stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+        time.sleep(0.5)
+
+    def mark(self, begin: bool):
+        if begin:
+            self.t0 = time.time()
+        else:
+            self.t1 = time.time()
+
+    def stop(self):
+        if self.proc is None:
+            return {"unavailable": "nvidia-smi not found"}
+        time.sleep(0.15)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.out.flush()
+        self.out.seek(0)
+        rows = [r.split(", ") for r in self.out.read().strip().splitlines()]
+        os.unlink(self.out.name)
+        rows = [r for r in rows if len(r) >= 10]
+        if len({r[1].strip() for r in rows}) > 1:
+            rows = [r for r in rows if r[1].strip() == str(self.gpu_index)]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        sm, smax, reasons, under = [], [], set(), 0
+        for r in rows:
+            try:
+                ts = datetime.datetime.strptime(r[0].strip(), "%Y/%m/%d %H:%M:%S.%f").timestamp()
+            except ValueError:
+                ts = None
+            if ts is not None and self.t0 and self.t1 and not (self.t0 - 0.15 <= ts <= self.t1 + 0.15):
+                continue
+            under += 1
+            try:
+                sm.append(float(r[2]))
+                smax.append(float(r[3]))
+            except ValueError:
+                pass
+            for n, v in zip(names, r[6:10]):
+                if v.strip().lower() == "active":
+                    reasons.add(n)
+        if not sm:
+            return {"unavailable": "no nvidia-smi sample inside the timed region", "samples": len(rows)}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax), "reasons": sorted(reasons),
+                "samples": under}
+
+
+# ---------------------------------------------------------------------------
+# the reference arm: the CPU oracle on the host cores
+# ---------------------------------------------------------------------------
+
+def run_reference(args):
+    if int(os.environ.get("RANK", "0")) != 0:
+        return 0
+    import oracle
+    import synth
+    oracle.build()
+    w = synth.WORKLOADS[WORKLOAD]
+    W, N = w["W"], w["N"]
+    # Calibrate, then size one step's sample so the whole run stays near two minutes.
+    cal = synth.workload_inputs(WORKLOAD, N=W * 4096)
+    t = time.perf_counter()
+    oracle.allreduce("fp32", "avg", "ring", cal)
+    per_elem = (time.perf_counter() - t) / (W * 4096)
+    budget = 120.0 / max(1, args.steps + args.warmup)
+    n = int(budget / per_elem) // (W * 1024) * (W * 1024)
+    n = max(W * 1024, min(N, n))
+    host = synth.workload_inputs(WORKLOAD, N=n)
+    for _ in range(args.warmup):
+        oracle.allreduce("fp32", "avg", "ring", host)
+    t = time.perf_counter()
+    for _ in range(args.steps):
+        oracle.allreduce("fp32", "avg", "ring", host)
+    dt = time.perf_counter() - t
+    gbs = 2 * W * n * 4 * args.steps / dt / 1e9
+    sample = f"first {n} of {N} elements per rank of {WORKLOAD} (W={W}), ring avg, one oracle call per step"
+    line = {
+        "impl": "reference", "metric": METRIC, "value": gbs, "unit": "GB/s", "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt / args.steps * 1e3,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+        "data": "synthetic", "config": workload_config(W, N),
+        "cpu_baseline": {"value": gbs, "unit": "GB/s", "cores": 1, "kind": "oracle", "sample": sample,
+                         "cpu": cpu_model(), "host_cores": os.cpu_count()},
+        "e2e": {"value": gbs, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line))
+    return 0
+
+
+def workload_config(W, N):
+    return {"workload": WORKLOAD, "W": W, "N_per_rank": N, "dtype": "fp32", "op": "avg", "algo": "ring",
+            "bytes_per_step": 2 * W * N * 4, "l2": "inputs larger than L2 (1 GiB per step vs 129 MB L2), no flush"}
+
+
+# ---------------------------------------------------------------------------
+# the CUDA path
+# ---------------------------------------------------------------------------
+
+def time_calls(fn, iters, flush=None):
+    """Median and mean device time (ms) of fn over iters calls, each bracketed
+    by its own events on the current stream; flush() runs outside the events."""
+    import torch
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(iters)]
+    for a, b in evs:
+        if flush is not None:
+            flush()
+        a.record()
+        fn()
+        b.record()
+    torch.cuda.synchronize()
+    ts = [a.elapsed_time(b) for a, b in evs]
+    return statistics.median(ts), statistics.mean(ts), min(ts), max(ts)
+
+
+def extras(mr, torch, dev):
+    """Size sweep (ring vs tree, warm and L2-flushed), the FSDP reduce-scatter and
+    all-gather, the integer all-reduce and fused-vs-unfused all-reduce."""
+    import numpy as np
+    import synth
+    out = {}
+    flush_buf = torch.empty(2 * L2_BYTES // 4 + 1024, dtype=torch.float32, device=dev)
+
+    def flush():
+        flush_buf.zero_()
+
+    sweep = []
+    W = 8
+    for N in synth.WORKLOADS["sweep_fp32_w8"]["Ns"]:
+        host = synth.workload_inputs("sweep_fp32_w8", N=N)
+        xs = [torch.from_numpy(h).to(dev) for h in host]
+        ys = [torch.empty_like(x) for x in xs]
+        row = {"N_per_rank": N, "bytes_per_rank": N * 4}
+        for algo in ("ring", "tree"):
+            def call():
+                mr.mr_allreduce(xs, ys, op="sum", algo=algo)
+            for _ in range(5):
+                call()
+            med, _, _, _ = time_calls(call, 30)
+            row[f"{algo}_us"] = med * 1e3
+            row[f"{algo}_gbs"] = 2 * W * N * 4 / (med * 1e-3) / 1e9
+            if 2 * W * N * 4 < 4 * L2_BYTES:
+                fmed, _, _, _ = time_calls(call, 30, flush)
+                row[f"{algo}_flushed_us"] = fmed * 1e3
+                row[f"{algo}_flushed_gbs"] = 2 * W * N * 4 / (fmed * 1e-3) / 1e9
+        sweep.append(row)
+        del xs, ys
+    out["sweep_fp32_w8_sum"] = sweep
+
+    # FSDP: reduce-scatter avg of bf16 gradients, all-gather of bf16 parameter shards
+    host = synth.workload_inputs("fsdp_bf16_w8")
+    W, N = len(host), host[0].size
+    xs = [torch.from_numpy(h.view(np.int16)).to(dev).view(torch.bfloat16) for h in host]
+    shards = [torch.empty(N // W, dtype=torch.bfloat16, device=dev) for _ in range(W)]
+    full = [torch.empty(N, dtype=torch.bfloat16, device=dev) for _ in range(W)]
+    rs = lambda: mr.mr_reduce_scatter(xs, shards, op="avg", algo="ring")  # noqa: E731
+    ag = lambda: mr.mr_all_gather(shards, full)  # noqa: E731
+    for _ in range(3):
+        rs()
+        ag()
+    rmed, _, _, _ = time_calls(rs, 20)
+    amed, _, _, _ = time_calls(ag, 20)
+    out["fsdp_bf16_w8"] = {
+        "reduce_scatter_us": rmed * 1e3, "reduce_scatter_gbs": (W + 1) * N * 2 / (rmed * 1e-3) / 1e9,
+        "all_gather_us": amed * 1e3, "all_gather_gbs": (W + 1) * N * 2 / (amed * 1e-3) / 1e9}
+    del xs, shards, full
+
+    # integer counts: W=16 int32
+    host = synth.workload_inputs("int_counts_w16")
+    W, N = len(host), host[0].size
+    xs = [torch.from_numpy(h).to(dev) for h in host]
+    ys = [torch.empty_like(x) for x in xs]
+    row = {}
+    for op in ("sum", "max"):
+        for algo in ("ring", "tree"):
+            f = lambda: mr.mr_allreduce(xs, ys, op=op, algo=algo)  # noqa: E731
+            f()
+            med, _, _, _ = time_calls(f, 20)
+            row[f"{op}_{algo}_gbs"] = 2 * W * N * 4 / (med * 1e-3) / 1e9
+    out["int_counts_w16"] = row
+    del xs, ys
+
+    # fused all-reduce against reduce-scatter followed by all-gather (DDP bucket)
+    host = synth.workload_inputs(WORKLOAD)
+    W, N = len(host), host[0].size
+    xs = [torch.from_numpy(h).to(dev) for h in host]
+    ys = [torch.empty_like(x) for x in xs]
+    sh = [torch.empty(N // W, device=dev) for _ in range(W)]
+    fused = lambda: mr.mr_allreduce(xs, ys, op="avg", algo="ring")  # noqa: E731
+
+    def unfused():
+        mr.mr_reduce_scatter(xs, sh, op="avg", algo="ring")
+        mr.mr_all_gather(sh, ys)
+    fused()
+    unfused()
+    fmed, _, _, _ = time_calls(fused, 20)
+    umed, _, _, _ = time_calls(unfused, 20)
+    out["fused_vs_unfused_ddp_bucket"] = {"fused_us": fmed * 1e3, "rs_then_ag_us": umed * 1e3,
+                                          "fused_bytes": 2 * W * N * 4, "unfused_bytes": (2 * W + 2) * N * 4}
+    return out
+
+
+def run_mine(args):
+    import torch
+
+    import collective_reduction_math_gb300 as mr
+    import synth
+    from collective_reduction_math_gb300 import _build
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    _build.build()
+    mr.load()
+
+    w = synth.WORKLOADS[WORKLOAD]
+    W, N = w["W"], w["N"]
+    bytes_step = 2 * W * N * 4
+    host = synth.workload_inputs(WORKLOAD, seed=0)
+    xs = [torch.from_numpy(h).to(dev) for h in host]
+    ys = [torch.empty_like(x) for x in xs]
+
+    def step():
+        mr.mr_allreduce(xs, ys, op="avg", algo="ring")
+
+    for _ in range(max(3, args.warmup)):
+        step()
+    torch.cuda.synchronize()
+    if dist:
+        dist.barrier()
+
+    gpu_index = local
+    vis = os.environ.get("CUDA_VISIBLE_DEVICES", "")
+    if vis and vis.split(",")[0].strip().isdigit():
+        gpu_index = int(vis.split(",")[local].strip())
+    sampler = ClockSampler(gpu_index)
+    sampler.start()
+    K = args.steps
+    per = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
+    t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    if dist:
+        dist.barrier()
+    launches0 = mr.mr_launch_count()
+    sampler.mark(True)
+    t_start.record()
+    for a, b in per:
+        a.record()
+        step()
+        b.record()
+    t_end.record()
+    torch.cuda.synchronize()
+    sampler.mark(False)
+    if dist:
+        dist.barrier()
+    launches = mr.mr_launch_count() - launches0
+    clocks = sampler.stop()
+    total_ms = t_start.elapsed_time(t_end)
+    kern_ms = statistics.mean(a.elapsed_time(b) for a, b in per)
+    if dist:
+        t = torch.tensor([total_ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        total_ms = float(t.item())
+    value = world * bytes_step * K / (total_ms * 1e-3) / 1e9
+
+    peak, peak_src = peaks()
+    achieved = bytes_step / (kern_ms * 1e-3) / 1e9
+    roofline = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
+                "traffic": profiled_traffic(), "peak_source": peak_src,
+                "kernel": "reduce_kernel<fp32, avg, ring, W<=8> (fused all-reduce)",
+                "algorithmic_bytes_per_launch": bytes_step, "kernel_ms_mean": kern_ms}
+
+    # end to end through the public API: pinned host inputs in, results out
+    e2e = None
+    if rank == 0 or world > 1:
+        hin = [torch.from_numpy(h).pin_memory() for h in host]
+        hout = [torch.empty(N, dtype=torch.float32).pin_memory() for _ in range(W)]
+
+        def e2e_step():
+            for x, h in zip(xs, hin):
+                x.copy_(h, non_blocking=True)
+            mr.mr_allreduce(xs, ys, op="avg", algo="ring")
+            for h, y in zip(hout, ys):
+                h.copy_(y, non_blocking=True)
+        e2e_step()
+        torch.cuda.synchronize()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        for _ in range(args.e2e_steps):
+            e2e_step()
+        b.record()
+        torch.cuda.synchronize()
+        e_ms = a.elapsed_time(b) / args.e2e_steps
+        e2e = {"value": bytes_step / (e_ms * 1e-3) / 1e9, "unit": "GB/s", "ms_per_step": e_ms,
+               "h2d_bytes_per_step": W * N * 4, "d2h_bytes_per_step": W * N * 4,
+               "steps": args.e2e_steps}
+        del hin, hout
+
+    extra = None
+    if rank == 0 and world == 1 and not args.no_extras:
+        del xs, ys
+        torch.cuda.empty_cache()
+        extra = extras(mr, torch, dev)
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        import oracle
+        oracle.build()
+        reps, t0 = 0, time.perf_counter()
+        while time.perf_counter() - t0 < 10.0:
+            oracle.allreduce("fp32", "avg", "ring", host)
+            reps += 1
+        dt = time.perf_counter() - t0
+        cpu = {"value": bytes_step * reps / dt / 1e9, "unit": "GB/s", "cores": 1, "kind": "oracle",
+               "sample": f"the full {WORKLOAD} workload (W={W}, 2^24 fp32 per rank), ring avg, "
+                         f"{reps} oracle calls in {dt:.1f} s, single-threaded",
+               "cpu": cpu_model(), "host_cores": os.cpu_count()}
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": K,
+            "warmup": max(3, args.warmup), "ms_per_step": total_ms / K, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+            "config": workload_config(W, N), "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
+            "gpu_launches": launches, "clocks": clocks, "device": torch.cuda.get_device_name(dev),
+            "extras": extra,
+        }
+        print(json.dumps(line))
+    if dist:
+        dist.barrier()
+        dist.destroy_process_group()
+    return 0
+
+
+def main():
+    args = parse_args()
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_mine(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,324 @@
+// api.cu -- the C ABI: argument validation, alias checks, the chunk-segment
+// planner and kernel dispatch.  See include/mr.h for the contract.
+#include <cuda_runtime.h>
+#include <stdarg.h>
+#include <stdint.h>
+#include <stdio.h>
+#include <stdlib.h>
+
+#include <algorithm>
+#include <atomic>
+#include <string>
+
+#include "mr.h"
+#include "mr_internal.h"
+#include "order.cuh"
+
+namespace {
+
+thread_local std::string g_last_error;
+std::atomic<unsigned long long> g_launches{0};
+
+int debug_level() {
+    static const int level = [] {
+        const char* e = getenv("MR_DEBUG");
+        return e ? atoi(e) : 0;
+    }();
+    return level;
+}
+
+mr_status_t fail(mr_status_t st, const char* fmt, ...) {
+    char buf[512];
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(buf, sizeof(buf), fmt, ap);
+    va_end(ap);
+    g_last_error = buf;
+    return st;
+}
+
+size_t elem_bytes(mr_dtype_t dt) { return dt == MR_BF16 ? 2u : 4u; }
+const char* dtype_name(mr_dtype_t dt) { return dt == MR_FP32 ? "fp32" : dt == MR_BF16 ? "bf16" : "int32"; }
+const char* op_name(mr_op_t op) {
+    static const char* n[] = {"sum", "prod", "min", "max", "avg"};
+    return n[op];
+}
+const char* algo_name(mr_algo_t a) { return a == MR_RING ? "ring" : "tree"; }
+
+// Streaming multiprocessors of the current device (cached per device).
+int sm_count() {
+    static std::atomic<int> cache[64];
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0) return 148;
+    if (dev < 64) {
+        int c = cache[dev].load(std::memory_order_relaxed);
+        if (c > 0) return c;
+    }
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) {
+        cudaGetLastError();
+        n = 148;
+    }
+    if (dev < 64) cache[dev].store(n, std::memory_order_relaxed);
+    return n;
+}
+
+mr_status_t check_common(const void* const* send, void* const* recv, int W, mr_dtype_t dtype) {
+    if (W < 1 || W > MR_MAX_RANKS)
+        return fail(MR_ERR_INVALID_ARGUMENT, "W = %d is outside [1, %d]", W, MR_MAX_RANKS);
+    if (dtype != MR_FP32 && dtype != MR_BF16 && dtype != MR_INT32)
+        return fail(MR_ERR_INVALID_ARGUMENT, "unknown dtype %d", (int)dtype);
+    if (!send || !recv) return fail(MR_ERR_INVALID_ARGUMENT, "send or recv pointer array is NULL");
+    return MR_OK;
+}
+
+mr_status_t check_pointers(const void* const* send, void* const* recv, int W, mr_dtype_t dtype) {
+    const uintptr_t a = elem_bytes(dtype) - 1;
+    for (int r = 0; r < W; ++r) {
+        if (!send[r]) return fail(MR_ERR_INVALID_ARGUMENT, "send[%d] is NULL", r);
+        if (!recv[r]) return fail(MR_ERR_INVALID_ARGUMENT, "recv[%d] is NULL", r);
+        if ((uintptr_t)send[r] & a)
+            return fail(MR_ERR_INVALID_ARGUMENT, "send[%d] is not aligned to its %s element", r, dtype_name(dtype));
+        if ((uintptr_t)recv[r] & a)
+            return fail(MR_ERR_INVALID_ARGUMENT, "recv[%d] is not aligned to its %s element", r, dtype_name(dtype));
+    }
+    return MR_OK;
+}
+
+mr_status_t check_op_algo(mr_op_t op, mr_algo_t algo) {
+    if (op < MR_SUM || op > MR_AVG) return fail(MR_ERR_INVALID_ARGUMENT, "unknown op %d", (int)op);
+    if (algo != MR_RING && algo != MR_TREE) return fail(MR_ERR_INVALID_ARGUMENT, "unknown algo %d", (int)algo);
+    return MR_OK;
+}
+
+// Overlap check over the 2W byte ranges.  Ranges of rank r's send and recv
+// buffers may overlap only when `inplace(r)` holds; every other pair of
+// non-empty ranges must be disjoint.  Sort by start, then sweep with the set of
+// ranges still open (which stays tiny when the buffers are disjoint).
+struct Range {
+    uintptr_t lo, hi;
+    int rank;
+    int is_recv;
+};
+
+template <class InPlace>
+mr_status_t check_alias(const void* const* send, size_t send_bytes, void* const* recv, size_t recv_bytes,
+                        int W, InPlace inplace) {
+    Range rs[2 * MR_MAX_RANKS];
+    int n = 0;
+    for (int r = 0; r < W; ++r) {
+        if (send_bytes) rs[n++] = {(uintptr_t)send[r], (uintptr_t)send[r] + send_bytes, r, 0};
+        if (recv_bytes) rs[n++] = {(uintptr_t)recv[r], (uintptr_t)recv[r] + recv_bytes, r, 1};
+    }
+    std::sort(rs, rs + n, [](const Range& a, const Range& b) { return a.lo < b.lo; });
+    int open[2 * MR_MAX_RANKS];
+    int nopen = 0;
+    for (int i = 0; i < n; ++i) {
+        int keep = 0;
+        for (int j = 0; j < nopen; ++j) {
+            const Range& o = rs[open[j]];
+            if (o.hi <= rs[i].lo) continue;        // closed before this one starts
+            open[keep++] = open[j];
+            const bool pair = o.rank == rs[i].rank && o.is_recv != rs[i].is_recv;
+            if (!(pair && inplace(o.rank)))
+                return fail(MR_ERR_ALIAS, "%s[%d] overlaps %s[%d] in a form that is not the allowed in-place one",
+                            o.is_recv ? "recv" : "send", o.rank, rs[i].is_recv ? "recv" : "send", rs[i].rank);
+        }
+        nopen = keep;
+        open[nopen++] = i;
+    }
+    return MR_OK;
+}
+
+// Segments of [0, N): each chunk k = [floor(kN/W), floor((k+1)N/W)), cut at
+// floor(N/2) for the tree algorithm (tree 1 below, tree 2 from there on).
+int plan_segments(int W, uint64_t N, mr_algo_t algo, mr::Segment* seg) {
+    int n = 0;
+    const uint64_t half = N / 2;
+    for (int k = 0; k < W; ++k) {
+        const uint64_t lo = mr::chunk_lo(W, N, k), hi = mr::chunk_lo(W, N, k + 1);
+        if (lo == hi) continue;
+        if (algo == MR_TREE && lo < half && half < hi) {
+            seg[n++] = {lo, half, lo, k, 0};
+            seg[n++] = {half, hi, lo, k, 1};
+        } else {
+            seg[n++] = {lo, hi, lo, k, (algo == MR_TREE && lo >= half) ? 1 : 0};
+        }
+    }
+    return n;
+}
+
+dim3 reduce_grid(const mr::ReduceParams& P, int lanes) {
+    uint64_t most = 0;
+    for (int i = 0; i < P.nseg; ++i) most = std::max(most, P.seg[i].hi - P.seg[i].lo);
+    const uint64_t units = P.vec ? (most + lanes - 1) / lanes : most;
+    const uint64_t need = std::max<uint64_t>(1, (units + mr::kThreads - 1) / mr::kThreads);
+    const int target = sm_count() * mr::kBlocksPerSm;
+    uint64_t gx = std::max(1, target / P.nseg);
+    gx = std::min(gx, need);
+    return dim3((unsigned)gx, (unsigned)P.nseg, 1);
+}
+
+cudaError_t launch_reduce(mr_dtype_t dtype, const mr::ReduceParams& P, mr_op_t op, mr_algo_t algo,
+                          dim3 grid, cudaStream_t s) {
+    switch (dtype) {
+        case MR_FP32: return mr::launch_reduce_fp32(P, op, algo, grid, s);
+        case MR_BF16: return mr::launch_reduce_bf16(P, op, algo, grid, s);
+        case MR_INT32: return mr::launch_reduce_int32(P, op, algo, grid, s);
+    }
+    return cudaErrorInvalidValue;
+}
+
+mr_status_t run_reduce(const char* what, int mode, const void* const* send, void* const* recv, int W, size_t N,
+                       mr_dtype_t dtype, mr_op_t op, mr_algo_t algo, void* stream) {
+    mr::ReduceParams P;
+    for (int r = 0; r < W; ++r) {
+        P.in[r] = send[r];
+        P.out[r] = recv[r];
+    }
+    P.W = W;
+    P.mode = mode;
+    P.scale = (float)(1.0 / (double)W);
+    P.nseg = plan_segments(W, N, algo, P.seg);
+    const int vb = mr::reduce_vector_bytes(W);
+    const int eb = (int)elem_bytes(dtype);
+    bool vec = true;
+    for (int r = 0; r < W; ++r)
+        vec = vec && ((uintptr_t)send[r] % vb == 0) && ((uintptr_t)recv[r] % vb == 0);
+    if (mode == mr::MODE_REDUCE_SCATTER) vec = vec && ((N / W) * eb) % vb == 0;
+    P.vec = vec ? 1 : 0;
+    const dim3 grid = reduce_grid(P, vb / eb);
+    const cudaError_t err = launch_reduce(dtype, P, op, algo, grid, (cudaStream_t)stream);
+    if (err != cudaSuccess)
+        return fail(MR_ERR_CUDA, "%s launch failed: %s", what, cudaGetErrorString(err));
+    g_launches.fetch_add(1, std::memory_order_relaxed);
+    if (debug_level() > 0)
+        fprintf(stderr, "[mr] %s dtype=%s op=%s algo=%s W=%d N=%zu segments=%d vector=%d grid=%ux%u threads=%d\n",
+                what, dtype_name(dtype), op_name(op), algo_name(algo), W, N, P.nseg, P.vec, grid.x, grid.y,
+                mr::kThreads);
+    return MR_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+mr_status_t mr_allreduce(const void* const* send, void* const* recv, int W, size_t N, mr_dtype_t dtype,
+                         mr_op_t op, mr_algo_t algo, void* stream) {
+    g_last_error.clear();
+    mr_status_t st = check_common(send, recv, W, dtype);
+    if (st == MR_OK) st = check_op_algo(op, algo);
+    if (st != MR_OK || N == 0) return st;
+    if ((st = check_pointers(send, recv, W, dtype)) != MR_OK) return st;
+    const size_t bytes = N * elem_bytes(dtype);
+    st = check_alias(send, bytes, recv, bytes, W, [&](int r) { return send[r] == recv[r]; });
+    if (st != MR_OK) return st;
+    return run_reduce("allreduce", mr::MODE_ALLREDUCE, send, recv, W, N, dtype, op, algo, stream);
+}
+
+mr_status_t mr_reduce_scatter(const void* const* send, void* const* recv, int W, size_t N, mr_dtype_t dtype,
+                              mr_op_t op, mr_algo_t algo, void* stream) {
+    g_last_error.clear();
+    mr_status_t st = check_common(send, recv, W, dtype);
+    if (st == MR_OK) st = check_op_algo(op, algo);
+    if (st != MR_OK) return st;
+    if (N % (size_t)W != 0)
+        return fail(MR_ERR_INVALID_ARGUMENT, "reduce_scatter needs N (%zu) divisible by W (%d)", N, W);
+    if (N == 0) return MR_OK;
+    if ((st = check_pointers(send, recv, W, dtype)) != MR_OK) return st;
+    const size_t b = elem_bytes(dtype), C = N / (size_t)W;
+    st = check_alias(send, N * b, recv, C * b, W, [&](int r) {
+        return (const char*)recv[r] == (const char*)send[r] + (size_t)r * C * b;
+    });
+    if (st != MR_OK) return st;
+    return run_reduce("reduce_scatter", mr::MODE_REDUCE_SCATTER, send, recv, W, N, dtype, op, algo, stream);
+}
+
+mr_status_t mr_all_gather(const void* const* send, void* const* recv, int W, size_t N, mr_dtype_t dtype,
+                          void* stream) {
+    g_last_error.clear();
+    mr_status_t st = check_common(send, recv, W, dtype);
+    if (st != MR_OK) return st;
+    if (N % (size_t)W != 0)
+        return fail(MR_ERR_INVALID_ARGUMENT, "all_gather needs N (%zu) divisible by W (%d)", N, W);
+    if (N == 0) return MR_OK;
+    if ((st = check_pointers(send, recv, W, dtype)) != MR_OK) return st;
+    const size_t b = elem_bytes(dtype), C = N / (size_t)W;
+    st = check_alias(send, C * b, recv, N * b, W, [&](int r) {
+        return (const char*)send[r] == (const char*)recv[r] + (size_t)r * C * b;
+    });
+    if (st != MR_OK) return st;
+
+    mr::GatherParams P;
+    for (int r = 0; r < W; ++r) {
+        P.in[r] = send[r];
+        P.out[r] = recv[r];
+    }
+    P.W = W;
+    P.C = C;
+    P.esize = (int)b;
+    bool vec = (C * b) % 16 == 0;
+    for (int r = 0; r < W; ++r) vec = vec && ((uintptr_t)send[r] % 16 == 0) && ((uintptr_t)recv[r] % 16 == 0);
+    P.vec = vec ? 1 : 0;
+    const uint64_t units = vec ? (C * b) / 16 : C;
+    const uint64_t need = std::max<uint64_t>(1, (units + mr::kThreads - 1) / mr::kThreads);
+    uint64_t gx = std::max(1, sm_count() * mr::kBlocksPerSm / W);
+    gx = std::min(gx, need);
+    const dim3 grid((unsigned)gx, (unsigned)W, 1);
+    const cudaError_t err = mr::launch_all_gather(P, grid, (cudaStream_t)stream);
+    if (err != cudaSuccess) return fail(MR_ERR_CUDA, "all_gather launch failed: %s", cudaGetErrorString(err));
+    g_launches.fetch_add(1, std::memory_order_relaxed);
+    if (debug_level() > 0)
+        fprintf(stderr, "[mr] all_gather dtype=%s W=%d N=%zu vector=%d grid=%ux%u threads=%d\n", dtype_name(dtype),
+                W, N, P.vec, grid.x, grid.y, mr::kThreads);
+    return MR_OK;
+}
+
+const char* mr_status_string(mr_status_t status) {
+    switch (status) {
+        case MR_OK: return "MR_OK";
+        case MR_ERR_INVALID_ARGUMENT: return "MR_ERR_INVALID_ARGUMENT";
+        case MR_ERR_UNSUPPORTED: return "MR_ERR_UNSUPPORTED";
+        case MR_ERR_ALIAS: return "MR_ERR_ALIAS";
+        case MR_ERR_CUDA: return "MR_ERR_CUDA";
+    }
+    return "MR_UNKNOWN_STATUS";
+}
+
+const char* mr_last_error(void) { return g_last_error.c_str(); }
+
+mr_status_t mr_plan_ring_order(int W, int k, int* order) {
+    g_last_error.clear();
+    if (W < 1 || W > MR_MAX_RANKS || k < 0 || k >= W || !order)
+        return fail(MR_ERR_INVALID_ARGUMENT, "mr_plan_ring_order: bad W, k or order");
+    for (int i = 0; i < W; ++i) order[i] = mr::ring_rank(W, k, i);
+    return MR_OK;
+}
+
+mr_status_t mr_plan_tree(int W, int which, int* parent, int* child, int* root) {
+    g_last_error.clear();
+    if (W < 1 || W > MR_MAX_RANKS || (which != 1 && which != 2) || !parent || !child || !root)
+        return fail(MR_ERR_INVALID_ARGUMENT, "mr_plan_tree: bad W, which or output pointer");
+    const int t = which - 1;
+    for (int p = 0; p < W; ++p) {
+        const int r = mr::tree_rank(W, t, p);
+        const int q = mr::tree_parent(W, p);
+        const int lo = mr::tree_lower_child(W, p), up = mr::tree_upper_child(W, p);
+        parent[r] = q < 0 ? -1 : mr::tree_rank(W, t, q);
+        int n = 0;
+        child[2 * r] = child[2 * r + 1] = -1;
+        if (lo >= 0) child[2 * r + n++] = mr::tree_rank(W, t, lo);
+        if (up >= 0) child[2 * r + n++] = mr::tree_rank(W, t, up);
+    }
+    *root = mr::tree_rank(W, t, 0);
+    return MR_OK;
+}
+
+size_t mr_chunk_lo(int W, size_t N, int k) {
+    if (W < 1 || k < 0 || k > W) return 0;
+    return (size_t)mr::chunk_lo(W, N, k);
+}
+
+unsigned long long mr_launch_count(void) { return g_launches.load(std::memory_order_relaxed); }
+
+}  // extern "C"

@@ -1,0 +1,324 @@
+// reduce_kernel.cuh -- the fused reduction kernel: all-reduce (reduce-scatter
+// and all-gather in one pass) and reduce-scatter over W rank buffers in one
+// GPU's HBM.
+//
+// Per element (post on NCCL all-reduce, "What all-reduce promises" and "The
+// ring, exactly as the kernel runs it"): read the W contributions, widen bf16
+// to fp32, pre-scale float avg by 1/W, combine them in the planned order in
+// registers, apply the postOp (bf16 rounding, integer avg divide), and store
+// the result to all W outputs (all-reduce) or to the owner's shard
+// (reduce-scatter).  Nothing is staged in memory between the reads and the
+// writes: the partial sum lives only in registers, the way the page's fused
+// receive-reduce-send primitives keep it in flight.
+//
+// Memory-bound: 2*W*N*b HBM bytes for all-reduce, (W+1)*N*b for
+// reduce-scatter, at most W-1 combines per element.  No tensor cores.
+//
+// Layout of the work: blockIdx.y picks a segment (one chunk, or a chunk cut at
+// the tree-1/tree-2 boundary), so the accumulation order is uniform across a
+// CTA.  blockIdx.x strides over the segment's aligned vectors; the unaligned
+// head and tail of a segment (fewer than one vector each), and whole segments
+// whose pointers are not vector-aligned, run the same arithmetic one element
+// per thread.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <stdint.h>
+
+#include <type_traits>
+
+#include "mr_internal.h"
+#include "order.cuh"
+
+namespace mr {
+
+// ---------------------------------------------------------------------------
+// Element types
+// ---------------------------------------------------------------------------
+
+template <int DT> struct Elem;
+template <> struct Elem<MR_FP32> { using raw_t = uint32_t; using acc_t = float;    static constexpr int kBytes = 4; };
+template <> struct Elem<MR_BF16> { using raw_t = uint16_t; using acc_t = float;    static constexpr int kBytes = 2; };
+template <> struct Elem<MR_INT32> { using raw_t = uint32_t; using acc_t = uint32_t; static constexpr int kBytes = 4; };
+
+// Total-order key of an fp32 value: a signed integer that orders -0 below +0
+// and otherwise follows the numeric order (NaN excluded).
+__device__ __forceinline__ int32_t f32_order_key(float x) {
+    int32_t b = __float_as_int(x);
+    return b ^ ((b >> 31) & 0x7FFFFFFF);
+}
+
+template <int DT, int OP> struct Arith {
+    using E = Elem<DT>;
+    using raw_t = typename E::raw_t;
+    using acc_t = typename E::acc_t;
+
+    // Read one contribution: widen, and pre-scale a float avg by fl32(1/W).
+    static __device__ __forceinline__ acc_t read(raw_t x, float s) {
+        if constexpr (DT == MR_INT32) {
+            return x;
+        } else {
+            float f = (DT == MR_FP32) ? __uint_as_float(x) : __uint_as_float((uint32_t)x << 16);
+            if constexpr (OP == MR_AVG) f = __fmul_rn(f, s);
+            return f;
+        }
+    }
+
+    static __device__ __forceinline__ acc_t combine(acc_t a, acc_t b) {
+        if constexpr (DT == MR_INT32) {
+            if constexpr (OP == MR_SUM || OP == MR_AVG) return a + b;   // wraps mod 2^32
+            if constexpr (OP == MR_PROD) return a * b;
+            if constexpr (OP == MR_MIN) return ((int32_t)b < (int32_t)a) ? b : a;
+            if constexpr (OP == MR_MAX) return ((int32_t)a < (int32_t)b) ? b : a;
+        } else {
+            if constexpr (OP == MR_SUM || OP == MR_AVG) return __fadd_rn(a, b);
+            if constexpr (OP == MR_PROD) return __fmul_rn(a, b);
+            if constexpr (OP == MR_MIN) return (f32_order_key(b) < f32_order_key(a)) ? b : a;
+            if constexpr (OP == MR_MAX) return (f32_order_key(a) < f32_order_key(b)) ? b : a;
+        }
+    }
+
+    // The postOp where the sum completes.
+    static __device__ __forceinline__ raw_t post(acc_t a, int W) {
+        if constexpr (DT == MR_FP32) return __float_as_uint(a);
+        if constexpr (DT == MR_BF16) return __bfloat16_as_ushort(__float2bfloat16_rn(a));
+        if constexpr (DT == MR_INT32) {
+            if constexpr (OP == MR_AVG) return (uint32_t)((int32_t)a / W);
+            return a;
+        }
+    }
+};
+
+// ---------------------------------------------------------------------------
+// The folds.  y[p] holds the contribution at order position p; only the
+// first W positions are valid.  All register indices are compile-time.
+// ---------------------------------------------------------------------------
+
+// Ring: a left fold in chunk order.
+template <class A, int WCAP>
+__device__ __forceinline__ typename A::acc_t fold_ring(const typename A::acc_t (&y)[WCAP], int W) {
+    typename A::acc_t a = y[0];
+#pragma unroll
+    for (int i = 1; i < WCAP; ++i)
+        if (i < W) a = A::combine(a, y[i]);
+    return a;
+}
+
+// Tree: subtotals level by level (lowest set bit 2, 4, ...), so every child is
+// complete before its parent uses it; each node takes its own value, then its
+// lower child's subtotal, then its upper child's; the root takes its one child.
+template <class A, int WCAP>
+__device__ __forceinline__ typename A::acc_t fold_tree(typename A::acc_t (&y)[WCAP], int W) {
+#pragma unroll
+    for (int b = 2; b < WCAP; b <<= 1) {
+#pragma unroll
+        for (int p = b; p < WCAP; p += 2 * b) {
+            if (p < W) {
+                typename A::acc_t a = A::combine(y[p], y[p - b / 2]);
+                bool taken = false;
+#pragma unroll
+                for (int h = b / 2; h >= 1; h >>= 1) {
+                    if (!taken && p + h < W) {
+                        a = A::combine(a, y[p + h]);
+                        taken = true;
+                    }
+                }
+                y[p] = a;
+            }
+        }
+    }
+    typename A::acc_t a = y[0];
+    bool taken = false;
+#pragma unroll
+    for (int h = WCAP / 2; h >= 1; h >>= 1) {
+        if (!taken && h < W) {
+            a = A::combine(a, y[h]);
+            taken = true;
+        }
+    }
+    return a;
+}
+
+template <class A, int ALGO, int WCAP>
+__device__ __forceinline__ typename A::acc_t fold(typename A::acc_t (&y)[WCAP], int W) {
+    if constexpr (ALGO == MR_RING) return fold_ring<A, WCAP>(y, W);
+    else return fold_tree<A, WCAP>(y, W);
+}
+
+// ---------------------------------------------------------------------------
+// Global memory access
+// ---------------------------------------------------------------------------
+
+template <int VB> struct Vec { uint32_t w[VB / 4]; };
+
+// Inputs are read once and never re-read: read-only path, no L1 allocation.
+template <int VB> __device__ __forceinline__ Vec<VB> load_vec(const char* p) {
+    Vec<VB> v;
+    if constexpr (VB == 16) {
+        asm("ld.global.nc.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
+            : "=r"(v.w[0]), "=r"(v.w[1]), "=r"(v.w[2]), "=r"(v.w[3]) : "l"(p));
+    } else if constexpr (VB == 8) {
+        asm("ld.global.nc.L1::no_allocate.v2.u32 {%0, %1}, [%2];" : "=r"(v.w[0]), "=r"(v.w[1]) : "l"(p));
+    } else {
+        asm("ld.global.nc.L1::no_allocate.u32 %0, [%1];" : "=r"(v.w[0]) : "l"(p));
+    }
+    return v;
+}
+
+// Outputs are written once: streaming (evict-first) stores.
+template <int VB> __device__ __forceinline__ void store_vec(char* p, const Vec<VB>& v) {
+    if constexpr (VB == 16) {
+        asm volatile("st.global.cs.v4.u32 [%0], {%1, %2, %3, %4};"
+                     :: "l"(p), "r"(v.w[0]), "r"(v.w[1]), "r"(v.w[2]), "r"(v.w[3]) : "memory");
+    } else if constexpr (VB == 8) {
+        asm volatile("st.global.cs.v2.u32 [%0], {%1, %2};" :: "l"(p), "r"(v.w[0]), "r"(v.w[1]) : "memory");
+    } else {
+        asm volatile("st.global.cs.u32 [%0], %1;" :: "l"(p), "r"(v.w[0]) : "memory");
+    }
+}
+
+template <class raw_t, int VB> __device__ __forceinline__ raw_t get_lane(const Vec<VB>& v, int l) {
+    if constexpr (sizeof(raw_t) == 4) return v.w[l];
+    else return (raw_t)(v.w[l >> 1] >> (16 * (l & 1)));
+}
+
+template <class raw_t, int VB> __device__ __forceinline__ void set_lane(Vec<VB>& v, int l, raw_t x) {
+    if constexpr (sizeof(raw_t) == 4) {
+        v.w[l] = x;
+    } else {
+        if (l & 1) v.w[l >> 1] |= (uint32_t)x << 16;
+        else v.w[l >> 1] = (uint32_t)x;
+    }
+}
+
+// ---------------------------------------------------------------------------
+// The kernel
+// ---------------------------------------------------------------------------
+
+// Rank at order position i of segment sg.
+template <int ALGO>
+__device__ __forceinline__ int order_rank(int W, const Segment& sg, int i) {
+    if constexpr (ALGO == MR_RING) return ring_rank(W, sg.k, i);
+    else return tree_rank(W, sg.tree, i);
+}
+
+template <int DT, int OP, int ALGO, int WCAP, int VB>
+__global__ void __launch_bounds__(kThreads, kBlocksPerSm)
+reduce_kernel(const __grid_constant__ ReduceParams P) {
+    using A = Arith<DT, OP>;
+    using raw_t = typename A::raw_t;
+    using acc_t = typename A::acc_t;
+    constexpr int EB = Elem<DT>::kBytes;
+    constexpr int LANES = VB / EB;
+
+    const Segment& sg = P.seg[blockIdx.y];
+    const int W = P.W;
+    const float s = P.scale;
+    const bool rs = (P.mode == MODE_REDUCE_SCATTER);
+
+    // Input pointers in this segment's accumulation order: in registers for
+    // up to 16 ranks, in a shared-memory table beyond that.
+    constexpr bool kTable = WCAP > 16;
+    __shared__ const char* table[kTable ? WCAP : 1];
+    const char* src[kTable ? 1 : WCAP];
+    if constexpr (kTable) {
+        if (threadIdx.x < W)
+            table[threadIdx.x] = static_cast<const char*>(P.in[order_rank<ALGO>(W, sg, threadIdx.x)]);
+        __syncthreads();
+    } else {
+#pragma unroll
+        for (int i = 0; i < WCAP; ++i)
+            src[i] = (i < W) ? static_cast<const char*>(P.in[order_rank<ALGO>(W, sg, i)]) : nullptr;
+    }
+    auto input = [&](int i) -> const char* {
+        if constexpr (kTable) return table[i];
+        else return src[i];
+    };
+
+    const uint64_t tid = (uint64_t)blockIdx.x * kThreads + threadIdx.x;
+    const uint64_t stride = (uint64_t)gridDim.x * kThreads;
+
+    // Vector part: vectors [va, vb) lie wholly inside [lo, hi).
+    uint64_t va = 0, vb = 0;
+    if (P.vec) {
+        va = (sg.lo + LANES - 1) / LANES;
+        vb = sg.hi / LANES;
+        if (va > vb) va = vb;
+    }
+    for (uint64_t v = va + tid; v < vb; v += stride) {
+        const uint64_t off = v * VB;
+        Vec<VB> raw[WCAP];
+#pragma unroll
+        for (int i = 0; i < WCAP; ++i)
+            if (i < W) raw[i] = load_vec<VB>(input(i) + off);
+        Vec<VB> res;
+#pragma unroll
+        for (int l = 0; l < LANES; ++l) {
+            acc_t y[WCAP];
+#pragma unroll
+            for (int i = 0; i < WCAP; ++i)
+                if (i < W) y[i] = A::read(get_lane<raw_t, VB>(raw[i], l), s);
+            set_lane<raw_t, VB>(res, l, A::post(fold<A, ALGO, WCAP>(y, W), W));
+        }
+        if (rs) {
+            store_vec<VB>(static_cast<char*>(P.out[sg.k]) + off - sg.out_lo * EB, res);
+        } else {
+#pragma unroll
+            for (int j = 0; j < WCAP; ++j)
+                if (j < W) store_vec<VB>(static_cast<char*>(P.out[j]) + off, res);
+        }
+    }
+
+    // Element part: the head [lo, va*LANES) and the tail [vb*LANES, hi), or the
+    // whole segment when the vector path is off.
+    uint64_t h0 = sg.lo, h1 = sg.hi, t0 = sg.hi, t1 = sg.hi;
+    if (P.vec && va < vb) {
+        h1 = va * LANES;
+        t0 = vb * LANES;
+    }
+#pragma unroll 1
+    for (int part = 0; part < 2; ++part) {
+        const uint64_t e0 = part ? t0 : h0, e1 = part ? t1 : h1;
+        for (uint64_t e = e0 + tid; e < e1; e += stride) {
+            acc_t y[WCAP];
+#pragma unroll
+            for (int i = 0; i < WCAP; ++i)
+                if (i < W) y[i] = A::read(__ldg(reinterpret_cast<const raw_t*>(input(i)) + e), s);
+            const raw_t r = A::post(fold<A, ALGO, WCAP>(y, W), W);
+            if (rs) {
+                static_cast<raw_t*>(P.out[sg.k])[e - sg.out_lo] = r;
+            } else {
+#pragma unroll
+                for (int j = 0; j < WCAP; ++j)
+                    if (j < W) static_cast<raw_t*>(P.out[j])[e] = r;
+            }
+        }
+    }
+}
+
+// Instantiate and launch the kernel for one element type.
+template <int DT>
+cudaError_t launch_reduce(const ReduceParams& P, int op, int algo, dim3 grid, cudaStream_t stream) {
+    auto go = [&](auto op_c, auto algo_c) -> cudaError_t {
+        constexpr int OP = decltype(op_c)::value;
+        constexpr int ALGO = decltype(algo_c)::value;
+        if (P.W <= 8) reduce_kernel<DT, OP, ALGO, 8, 16><<<grid, kThreads, 0, stream>>>(P);
+        else if (P.W <= 16) reduce_kernel<DT, OP, ALGO, 16, 16><<<grid, kThreads, 0, stream>>>(P);
+        else reduce_kernel<DT, OP, ALGO, 64, 4><<<grid, kThreads, 0, stream>>>(P);
+        return cudaGetLastError();
+    };
+    auto with_algo = [&](auto op_c) -> cudaError_t {
+        if (algo == MR_RING) return go(op_c, std::integral_constant<int, MR_RING>{});
+        return go(op_c, std::integral_constant<int, MR_TREE>{});
+    };
+    switch (op) {
+        case MR_SUM: return with_algo(std::integral_constant<int, MR_SUM>{});
+        case MR_PROD: return with_algo(std::integral_constant<int, MR_PROD>{});
+        case MR_MIN: return with_algo(std::integral_constant<int, MR_MIN>{});
+        case MR_MAX: return with_algo(std::integral_constant<int, MR_MAX>{});
+        case MR_AVG: return with_algo(std::integral_constant<int, MR_AVG>{});
+    }
+    return cudaErrorInvalidValue;
+}
+
+}  // namespace mr

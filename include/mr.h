@@ -1,0 +1,137 @@
+/*
+ * mr.h -- collective reduction math on one GPU.
+ *
+ * The element-wise arithmetic of all-reduce, reduce-scatter and all-gather over
+ * W rank buffers that all live in the HBM of one GPU ("simulated ranks").  No
+ * byte crosses to another GPU: rank r is simply the r-th pointer of an array.
+ *
+ * Sources (page title, section):
+ *   [AR]   post on NCCL all-reduce (rakshithvasudev.github.io), "What all-reduce
+ *          promises": one same-shaped tensor per rank, combined element-wise
+ *          with sum, prod, min, max or avg; every rank ends with the identical
+ *          result.  avg pre-scales each float contribution by 1/n as it is read
+ *          and divides an integer sum once at the end.
+ *   [RING] same post, "The ring, exactly as the kernel runs it": the buffer is
+ *          cut into n chunks; chunk k's running total starts on one rank and
+ *          gains one neighbour's contribution per hop over n-1 hops; all-reduce
+ *          is reduce-scatter followed by all-gather, fused.
+ *   [TREE] same post, "The double binary tree": the bit-trick binary tree, the
+ *          mirrored (even n) or shifted (odd n) second tree, each tree carrying
+ *          half of the buffer.
+ *   [FSDP] FSDP collectives 101, "All-gather: everyone shows their piece" and
+ *          "Why backward needs a different collective": all-gather concatenates
+ *          the shards; reduce-scatter leaves rank k holding slice k of the
+ *          reduced result.
+ *   [EQ2]  NCCL M2N, Eq. (2), "Local shard bounds": chunk k of an N-element
+ *          buffer split W ways starts at floor(k*N/W).
+ *
+ * Conventions shared by all three collectives:
+ *   - send and recv are HOST arrays of W DEVICE pointers.  The library copies
+ *     both arrays into the kernel's parameter block before it returns, so the
+ *     caller may free or reuse them immediately.
+ *   - Buffers are dense 1-D arrays of `dtype` elements: fp32, bf16 (IEEE
+ *     bfloat16 bit patterns) or int32.  Every pointer must be non-NULL and
+ *     aligned to its element size; 16-byte alignment enables the vectorised
+ *     path, anything else runs the element-wise path on the GPU.
+ *   - Arithmetic: fp32 and bf16 accumulate in fp32, one IEEE operation per
+ *     step, round to nearest even, no fused multiply-add; bf16 results are
+ *     rounded to bf16 once, at the end.  int32 sum and prod wrap modulo 2^32;
+ *     int32 avg is the C truncating divide of the wrapped sum by W.  min and
+ *     max order -0 below +0.
+ *   - Accumulation order (this decides float rounding): MR_RING folds chunk k
+ *     of the buffer (elements [floor(kN/W), floor((k+1)N/W))) in rank order
+ *     k+1, k+2, ..., k (mod W).  MR_TREE reduces elements [0, floor(N/2)) up
+ *     tree 1 and the rest up tree 2, each node adding its children's subtotals
+ *     to its own contribution (own value first, then the children in tree-1
+ *     position order).
+ *   - Work is enqueued on `stream` (a cudaStream_t; NULL is the legacy default
+ *     stream) and is asynchronous: the call never synchronises, allocates no
+ *     device memory and creates no streams.  Execution errors surface at the
+ *     caller's next synchronisation.  N == 0 launches nothing and returns MR_OK.
+ *   - Errors in arguments return at once and launch nothing; a failed launch
+ *     returns MR_ERR_CUDA.  mr_last_error() then describes the failure.
+ *   - Allowed aliasing (in place) is listed per call; any other overlap between
+ *     the 2W byte ranges returns MR_ERR_ALIAS.
+ */
+#ifndef MR_H
+#define MR_H
+
+#include <stddef.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define MR_MAX_RANKS 64
+
+typedef enum { MR_FP32 = 0, MR_BF16 = 1, MR_INT32 = 2 } mr_dtype_t;
+typedef enum { MR_SUM = 0, MR_PROD = 1, MR_MIN = 2, MR_MAX = 3, MR_AVG = 4 } mr_op_t;
+typedef enum { MR_RING = 0, MR_TREE = 1 } mr_algo_t;
+typedef enum {
+    MR_OK = 0,
+    MR_ERR_INVALID_ARGUMENT = 1, /* W out of [1, 64], NULL or misaligned pointer,
+                                    N % W != 0 where required, bad enum value */
+    MR_ERR_UNSUPPORTED = 2,      /* reserved: a valid request this build cannot run */
+    MR_ERR_ALIAS = 3,            /* buffers overlap other than in an allowed form */
+    MR_ERR_CUDA = 4              /* the CUDA runtime refused the launch */
+} mr_status_t;
+
+/*
+ * All-reduce [AR][RING][TREE]: recv[j][e] = result(e) for every rank j.
+ *   send[r], recv[r]: N elements each; any N >= 0 (chunks by [EQ2]).
+ *   In place: recv[r] == send[r] for every r.
+ * One kernel reads W*N and writes W*N elements (reduce-scatter and all-gather
+ * fused into one pass).
+ */
+mr_status_t mr_allreduce(const void* const* send, void* const* recv, int W, size_t N,
+                         mr_dtype_t dtype, mr_op_t op, mr_algo_t algo, void* stream);
+
+/*
+ * Reduce-scatter [FSDP][RING][TREE]: recv[k][i] = result(k*C + i), C = N / W.
+ *   send[r]: N elements; recv[k]: C elements (chunk k).  N % W == 0 required.
+ *   The element order of `result` is the all-reduce's (same chunks, same
+ *   tree split), so reduce-scatter followed by all-gather equals all-reduce
+ *   bit for bit.
+ *   In place: recv[r] == send[r] + r*C (in elements) for every r.
+ */
+mr_status_t mr_reduce_scatter(const void* const* send, void* const* recv, int W, size_t N,
+                              mr_dtype_t dtype, mr_op_t op, mr_algo_t algo, void* stream);
+
+/*
+ * All-gather [FSDP]: recv[j][k*C + i] = send[k][i] for every j, C = N / W.
+ *   send[k]: C elements (shard k); recv[j]: N elements.  N % W == 0 required.
+ *   A pure copy: no arithmetic.
+ *   In place: send[r] == recv[r] + r*C (in elements) for every r.
+ */
+mr_status_t mr_all_gather(const void* const* send, void* const* recv, int W, size_t N,
+                          mr_dtype_t dtype, void* stream);
+
+/* A static, human-readable name of a status code. */
+const char* mr_status_string(mr_status_t status);
+
+/* Detail of the last non-OK status returned on the calling thread ("" if none).
+ * The string is owned by the library and valid until the thread's next call. */
+const char* mr_last_error(void);
+
+/*
+ * Planner queries (host only; no GPU needed).  They expose the orders the
+ * kernels use.
+ *   mr_plan_ring_order: order[0..W-1] = the ranks that chunk k visits [RING].
+ *   mr_plan_tree: tree `which` (1 or 2) [TREE]; parent[r] (-1 at the root) and
+ *     child[2r], child[2r+1] (-1 if absent, tree-1 position order).  Returns
+ *     the root rank in *root.
+ *   mr_chunk_lo: floor(k*N/W) [EQ2].
+ */
+mr_status_t mr_plan_ring_order(int W, int k, int* order);
+mr_status_t mr_plan_tree(int W, int which, int* parent, int* child, int* root);
+size_t mr_chunk_lo(int W, size_t N, int k);
+
+/* Number of kernels this library has launched in this process (all threads,
+ * all devices).  Lets a caller count the GPU launches inside a timed region. */
+unsigned long long mr_launch_count(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif

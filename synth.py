@@ -54,14 +54,25 @@ def normal(seed: int, W: int, N: int, sigma: float, dtype: str = "fp32", tag: in
     return out
 
 
+def near_one(seed: int, W: int, N: int, dtype: str = "fp32", tag: int = TAG_GRAD):
+    """W buffers uniform in [0.5, 1.5) (products of up to 64 stay finite)."""
+    out = []
+    for r in range(W):
+        z = _rng(seed, tag, r).uniform(0.5, 1.5, size=N).astype(np.float32)
+        out.append(z if dtype == "fp32" else _to_bf16_bits(z))
+    return out
+
+
 def random_values(seed: int, W: int, N: int, dtype: str, kind: str = "normal", tag: int = TAG_GRAD):
-    """Generic test data: 'normal' (sigma 1), 'small_int' ([-8, 8]) or 'int'
-    ([-1000, 1000] for int32)."""
+    """Generic test data.  int32: uniform in [-1000, 1000].  Floats: 'normal'
+    (sigma 1), 'small_int' (integers in [-8, 8]) or 'near_one' ([0.5, 1.5))."""
     if dtype == "int32":
         return uniform_int(seed, W, N, -1000, 1000, "int32", tag)
     if kind == "small_int":
         vals = uniform_int(seed, W, N, -8, 8, "fp32", tag)
         return vals if dtype == "fp32" else [_to_bf16_bits(v) for v in vals]
+    if kind == "near_one":
+        return near_one(seed, W, N, dtype, tag)
     return normal(seed, W, N, 1.0, dtype, tag)
 
 

@@ -1,0 +1,144 @@
+"""The C-ABI boundary on the host: the library loads, exports every symbol
+include/mr.h declares, exposes the planner's orders, and rejects bad
+arguments before touching the GPU."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from golden_io import read_tree
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def _gpu_visible():
+    import torch
+    return torch.cuda.is_available() or os.path.exists("/dev/nvidia0")
+
+
+# These tests hand the library fake device addresses that must never be
+# dereferenced; they run only where no GPU exists, so a regression in argument
+# checking can never turn into a launch on bogus memory.
+pytestmark = pytest.mark.skipif(_gpu_visible(), reason="host-only checks with fake device addresses")
+
+
+@pytest.fixture(scope="module")
+def mr():
+    import __graft_entry__
+    __graft_entry__.build()
+    import collective_reduction_math_gb300 as m
+    m.load()
+    return m
+
+
+def _declared_functions():
+    names = set()
+    include = os.path.join(ROOT, "include")
+    for fn in os.listdir(include):
+        if fn.endswith(".h"):
+            text = open(os.path.join(include, fn)).read()
+            text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+            names |= set(re.findall(r"\b(mr_[a-z0-9_]+)\s*\(", text))
+    return sorted(names)
+
+
+def test_exports_every_declared_symbol(mr):
+    names = _declared_functions()
+    assert {"mr_allreduce", "mr_reduce_scatter", "mr_all_gather", "mr_status_string", "mr_last_error"} <= set(names)
+    lib = ctypes.CDLL(mr.LIB_PATH)
+    for n in names:
+        assert hasattr(lib, n), n
+
+
+def test_status_strings(mr):
+    assert mr.mr_status_string(0) == "MR_OK"
+    assert mr.mr_status_string(3) == "MR_ERR_ALIAS"
+    assert mr.mr_status_string(4) == "MR_ERR_CUDA"
+
+
+def test_ring_order(mr, oracle_mod):
+    for W in (1, 2, 3, 8, 16, 64):
+        for k in range(W):
+            assert mr.mr_plan_ring_order(W, k) == oracle_mod.ring_order(W, k)
+    assert mr.mr_plan_ring_order(4, 0) == [1, 2, 3, 0]
+
+
+def test_tree_matches_diagram_and_oracle(mr, oracle_mod):
+    parent, kids = read_tree("tree14.txt")
+    root, p, c = mr.mr_plan_tree(14, 1)
+    assert (root, p, c) == (0, parent, kids)
+    for W in range(1, 65):
+        for which in (1, 2):
+            assert mr.mr_plan_tree(W, which) == oracle_mod.tree(W, which), (W, which)
+
+
+def test_chunk_lo(mr):
+    for W in (1, 3, 8, 64):
+        for N in (0, 5, 4096, 2**40 + 7):
+            assert [mr.mr_chunk_lo(W, N, k) for k in range(W + 1)] == [(k * N) // W for k in range(W + 1)]
+
+
+def _arr(vals):
+    return (ctypes.c_void_p * len(vals))(*vals)
+
+
+def _call_ar(lib, send, recv, W, N, dtype=0, op=0, algo=0):
+    return lib.mr_allreduce(_arr(send), _arr(recv), W, N, dtype, op, algo, None)
+
+
+def test_argument_errors(mr):
+    lib = mr.load()
+    base = 1 << 40                      # never dereferenced: every call below fails validation
+    send = [base + r * (1 << 20) for r in range(4)]
+    recv = [base + (1 << 30) + r * (1 << 20) for r in range(4)]
+    assert _call_ar(lib, send, recv, 0, 16) == 1
+    assert _call_ar(lib, send, recv, 65, 16) == 1
+    assert _call_ar(lib, send, recv, 4, 16, dtype=3) == 1
+    assert _call_ar(lib, send, recv, 4, 16, op=5) == 1
+    assert _call_ar(lib, send, recv, 4, 16, algo=2) == 1
+    assert "algo" in mr.mr_last_error()
+    assert _call_ar(lib, send[:3] + [0], recv, 4, 16) == 1
+    assert "send[3]" in mr.mr_last_error()
+    assert _call_ar(lib, send, recv[:2] + [recv[2] + 2] + recv[3:], 4, 16) == 1     # misaligned fp32
+    assert _call_ar(lib, send, recv[:2] + [recv[2] + 1] + recv[3:], 4, 16, dtype=1) == 1  # misaligned bf16
+    assert lib.mr_allreduce(None, _arr(recv), 4, 16, 0, 0, 0, None) == 1
+    # N == 0 is a no-op that needs no GPU
+    assert _call_ar(lib, send, recv, 4, 0) == 0
+    # reduce-scatter / all-gather need N % W == 0
+    assert lib.mr_reduce_scatter(_arr(send), _arr(recv), 4, 18, 0, 0, 0, None) == 1
+    assert lib.mr_all_gather(_arr(send), _arr(recv), 4, 18, 0, None) == 1
+    assert "divisible" in mr.mr_last_error()
+
+
+def test_alias_rules(mr):
+    lib = mr.load()
+    W, N, b = 4, 1024, 4
+    base = 1 << 40
+    send = [base + r * N * b for r in range(W)]           # contiguous, disjoint
+    other = [base + (1 << 30) + r * N * b for r in range(W)]
+    # all-reduce: recv[r] == send[r] is allowed (it then needs a GPU: not run here)
+    # any other overlap is refused
+    shifted = [s + 64 for s in send]
+    assert _call_ar(lib, send, shifted, W, N) == 3
+    assert _call_ar(lib, send, [other[0]] * W, W, N) == 3              # outputs overlap each other
+    assert _call_ar(lib, send, [other[0], send[0]] + other[2:], W, N) == 3   # rank 1 writes rank 0's input
+    assert _call_ar(lib, [send[0], send[0]] + send[2:], other, W, N) == 3  # inputs overlap
+    # reduce-scatter: recv[r] == send[r] + r*C is the in-place form; recv[r] == send[r] is not
+    C = N // W
+    assert lib.mr_reduce_scatter(_arr(send), _arr(send), W, N, 0, 0, 0, None) == 3
+    # all-gather: send[r] == recv[r] + r*C is the in-place form; send[r] == recv[r] for r > 0 is not
+    assert lib.mr_all_gather(_arr(send), _arr(send), W, N, 0, None) == 3
+    assert "overlaps" in mr.mr_last_error()
+    _ = C
+
+
+def test_valid_call_without_gpu_reports_cuda_error(mr):
+    """With no usable GPU the launch itself fails: the call returns MR_ERR_CUDA
+    with the runtime's message instead of falling back to anything."""
+    lib = mr.load()
+    base = 1 << 40
+    send = [base + r * 4096 for r in range(2)]
+    recv = [base + (1 << 30) + r * 4096 for r in range(2)]
+    assert _call_ar(lib, send, recv, 2, 1024) == 4
+    assert "launch failed" in mr.mr_last_error()
