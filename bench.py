@@ -48,6 +48,12 @@ def parse_args():
     p.add_argument("--no-extras", action="store_true", help="skip the size sweep and the other workloads")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--e2e-steps", type=int, default=20)
+    p.add_argument("--workload", default=WORKLOAD, help="a workload of synth.WORKLOADS (default: the headline)")
+    p.add_argument("--collective", choices=["allreduce", "reduce_scatter", "all_gather"], default=None,
+                   help="the collective timed as one step (default: the workload's own)")
+    p.add_argument("--op", default=None)
+    p.add_argument("--algo", default="ring")
+    p.add_argument("--n", type=int, default=None, help="elements per rank (sweep workload)")
     return p.parse_args()
 
 
@@ -209,8 +215,10 @@ def run_reference(args):
 
 
 def workload_config(W, N):
-    return {"workload": WORKLOAD, "W": W, "N_per_rank": N, "dtype": "fp32", "op": "avg", "algo": "ring",
-            "bytes_per_step": 2 * W * N * 4, "l2": "inputs larger than L2 (1 GiB per step vs 129 MB L2), no flush"}
+    """The headline workload's config (the same keys the GPU arm reports)."""
+    return {"workload": WORKLOAD, "collective": "allreduce", "kernel": "fused all-reduce", "W": W,
+            "N_per_rank": N, "dtype": "fp32", "op": "avg", "algo": "ring", "bytes_per_step": 2 * W * N * 4,
+            "l2": "inputs larger than L2, no flush"}
 
 
 # ---------------------------------------------------------------------------
@@ -218,10 +226,14 @@ def workload_config(W, N):
 # ---------------------------------------------------------------------------
 
 def time_calls(fn, iters, flush=None):
-    """Median and mean device time (ms) of fn over iters calls, each bracketed
-    by its own events on the current stream; flush() runs outside the events."""
+    """Median, mean, min and max device time (ms) of fn over iters calls, each
+    bracketed by its own events on the current stream; flush() runs outside
+    the events.  The stream is first held by a device-side sleep while the
+    host enqueues every call, so small calls are timed on the device rather
+    than at the host's launch rate."""
     import torch
     evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(iters)]
+    torch.cuda._sleep(20_000_000)
     for a, b in evs:
         if flush is not None:
             flush()
@@ -231,6 +243,20 @@ def time_calls(fn, iters, flush=None):
     torch.cuda.synchronize()
     ts = [a.elapsed_time(b) for a, b in evs]
     return statistics.median(ts), statistics.mean(ts), min(ts), max(ts)
+
+
+def host_call_us(fn, iters=300):
+    """Host-side cost of one call (launch through the Python binding), with the
+    device kept ahead by a sleep so the host never waits on it."""
+    import torch
+    torch.cuda.synchronize()
+    torch.cuda._sleep(100_000_000)
+    t = time.perf_counter()
+    for _ in range(iters):
+        fn()
+    dt = time.perf_counter() - t
+    torch.cuda.synchronize()
+    return dt / iters * 1e6
 
 
 def extras(mr, torch, dev):
@@ -263,6 +289,8 @@ def extras(mr, torch, dev):
                 fmed, _, _, _ = time_calls(call, 30, flush)
                 row[f"{algo}_flushed_us"] = fmed * 1e3
                 row[f"{algo}_flushed_gbs"] = 2 * W * N * 4 / (fmed * 1e-3) / 1e9
+        if N == (1 << 10):
+            row["host_call_us"] = host_call_us(lambda: mr.mr_allreduce(xs, ys, op="sum", algo="ring"))
         sweep.append(row)
         del xs, ys
     out["sweep_fp32_w8_sum"] = sweep
@@ -320,11 +348,68 @@ def extras(mr, torch, dev):
     return out
 
 
+class Step:
+    """One step of a workload on the GPU: device buffers, the call, its bytes."""
+
+    DEFAULTS = {"small_int_fp32_w2": ("allreduce", "sum"), "ddp_bucket_fp32_w8": ("allreduce", "avg"),
+                "fsdp_bf16_w8": ("reduce_scatter", "avg"), "int_counts_w16": ("allreduce", "sum"),
+                "sweep_fp32_w8": ("allreduce", "sum")}
+
+    def __init__(self, args, mr, torch, dev):
+        import numpy as np
+        import synth
+        self.workload = args.workload
+        w = synth.WORKLOADS[self.workload]
+        self.collective, op = self.DEFAULTS[self.workload]
+        self.collective = args.collective or self.collective
+        self.op = args.op or op
+        self.algo = args.algo
+        self.W = W = w["W"]
+        self.N = N = args.n or w.get("N") or w["Ns"][-1]
+        self.dtype = w["dtype"]
+        tdt = {"fp32": torch.float32, "bf16": torch.bfloat16, "int32": torch.int32}[self.dtype]
+        b = 2 if self.dtype == "bf16" else 4
+        C = N // W
+
+        def dev_t(h):
+            return torch.from_numpy(h.view(np.int16) if self.dtype == "bf16" else h).to(dev).view(tdt)
+
+        if self.collective == "all_gather":
+            self.host_in = synth.workload_param_shards(self.workload, N=N) if "param_dist" in w else \
+                [h[:C].copy() for h in synth.workload_inputs(self.workload, N=N)]
+            self.xs = [dev_t(h) for h in self.host_in]
+            self.ys = [torch.empty(N, dtype=tdt, device=dev) for _ in range(W)]
+            self.bytes = (1 + W) * N * b
+            self.call = lambda: mr.mr_all_gather(self.xs, self.ys)
+        else:
+            self.host_in = synth.workload_inputs(self.workload, N=N)
+            self.xs = [dev_t(h) for h in self.host_in]
+            if self.collective == "allreduce":
+                self.ys = [torch.empty_like(x) for x in self.xs]
+                self.bytes = 2 * W * N * b
+                self.call = lambda: mr.mr_allreduce(self.xs, self.ys, op=self.op, algo=self.algo)
+            else:
+                self.ys = [torch.empty(C, dtype=tdt, device=dev) for _ in range(W)]
+                self.bytes = (W + 1) * N * b
+                self.call = lambda: mr.mr_reduce_scatter(self.xs, self.ys, op=self.op, algo=self.algo)
+        self.in_bytes = sum(x.numel() * b for x in self.xs)
+        self.out_bytes = sum(y.numel() * b for y in self.ys)
+
+    def config(self):
+        kernel = {"allreduce": "fused all-reduce", "reduce_scatter": "reduce-scatter",
+                  "all_gather": "all-gather"}[self.collective]
+        l2 = ("inputs larger than L2, no flush" if self.in_bytes + self.out_bytes > 4 * L2_BYTES
+              else "working set within 4x L2: warm-cache figure")
+        return {"workload": self.workload, "collective": self.collective, "kernel": kernel, "W": self.W,
+                "N_per_rank": self.N, "dtype": self.dtype, "op": self.op if self.collective != "all_gather" else None,
+                "algo": self.algo if self.collective != "all_gather" else None, "bytes_per_step": self.bytes,
+                "l2": l2}
+
+
 def run_mine(args):
     import torch
 
     import collective_reduction_math_gb300 as mr
-    import synth
     from collective_reduction_math_gb300 import _build
 
     world = int(os.environ.get("WORLD_SIZE", "1"))
@@ -339,15 +424,13 @@ def run_mine(args):
     _build.build()
     mr.load()
 
-    w = synth.WORKLOADS[WORKLOAD]
-    W, N = w["W"], w["N"]
-    bytes_step = 2 * W * N * 4
-    host = synth.workload_inputs(WORKLOAD, seed=0)
-    xs = [torch.from_numpy(h).to(dev) for h in host]
-    ys = [torch.empty_like(x) for x in xs]
-
-    def step():
-        mr.mr_allreduce(xs, ys, op="avg", algo="ring")
+    S = Step(args, mr, torch, dev)
+    W, N = S.W, S.N
+    bytes_step = S.bytes
+    host = S.host_in
+    xs, ys = S.xs, S.ys
+    step = S.call
+    headline = args.workload == WORKLOAD and S.collective == "allreduce" and S.op == "avg" and S.algo == "ring"
 
     for _ in range(max(3, args.warmup)):
         step()
@@ -392,22 +475,23 @@ def run_mine(args):
     peak, peak_src = peaks()
     achieved = bytes_step / (kern_ms * 1e-3) / 1e9
     roofline = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
-                "traffic": profiled_traffic(), "peak_source": peak_src,
-                "kernel": "reduce_kernel<fp32, avg, ring, W<=8> (fused all-reduce)",
-                "algorithmic_bytes_per_launch": bytes_step, "kernel_ms_mean": kern_ms}
+                "traffic": profiled_traffic() if headline else None, "peak_source": peak_src,
+                "kernel": S.config()["kernel"], "algorithmic_bytes_per_launch": bytes_step,
+                "kernel_ms_mean": kern_ms}
 
     # end to end through the public API: pinned host inputs in, results out
     e2e = None
     if rank == 0 or world > 1:
-        hin = [torch.from_numpy(h).pin_memory() for h in host]
-        hout = [torch.empty(N, dtype=torch.float32).pin_memory() for _ in range(W)]
+        import numpy as np
+        hin = [torch.from_numpy(np.ascontiguousarray(h).view(np.uint8)).pin_memory() for h in host]
+        hout = [torch.empty(y.numel() * y.element_size(), dtype=torch.uint8).pin_memory() for y in ys]
 
         def e2e_step():
             for x, h in zip(xs, hin):
-                x.copy_(h, non_blocking=True)
-            mr.mr_allreduce(xs, ys, op="avg", algo="ring")
+                x.view(torch.uint8).copy_(h, non_blocking=True)
+            step()
             for h, y in zip(hout, ys):
-                h.copy_(y, non_blocking=True)
+                h.copy_(y.view(torch.uint8), non_blocking=True)
         e2e_step()
         torch.cuda.synchronize()
         a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
@@ -418,18 +502,18 @@ def run_mine(args):
         torch.cuda.synchronize()
         e_ms = a.elapsed_time(b) / args.e2e_steps
         e2e = {"value": bytes_step / (e_ms * 1e-3) / 1e9, "unit": "GB/s", "ms_per_step": e_ms,
-               "h2d_bytes_per_step": W * N * 4, "d2h_bytes_per_step": W * N * 4,
+               "h2d_bytes_per_step": S.in_bytes, "d2h_bytes_per_step": S.out_bytes,
                "steps": args.e2e_steps}
         del hin, hout
 
     extra = None
-    if rank == 0 and world == 1 and not args.no_extras:
+    if rank == 0 and world == 1 and not args.no_extras and headline:
         del xs, ys
         torch.cuda.empty_cache()
         extra = extras(mr, torch, dev)
 
     cpu = None
-    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+    if rank == 0 and world == 1 and not args.no_cpu_baseline and headline:
         import oracle
         oracle.build()
         reps, t0 = 0, time.perf_counter()
@@ -446,8 +530,9 @@ def run_mine(args):
         line = {
             "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": K,
             "warmup": max(3, args.warmup), "ms_per_step": total_ms / K, "higher_is_better": True,
-            "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
-            "config": workload_config(W, N), "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f32" if S.dtype != "int32" else "i32",
+            "data": "synthetic",
+            "config": S.config(), "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
             "gpu_launches": launches, "clocks": clocks, "device": torch.cuda.get_device_name(dev),
             "extras": extra,
         }

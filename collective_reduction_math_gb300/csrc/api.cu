@@ -148,15 +148,28 @@ int plan_segments(int W, uint64_t N, mr_algo_t algo, mr::Segment* seg) {
     return n;
 }
 
-dim3 reduce_grid(const mr::ReduceParams& P, int lanes) {
-    uint64_t most = 0;
-    for (int i = 0; i < P.nseg; ++i) most = std::max(most, P.seg[i].hi - P.seg[i].lo);
-    const uint64_t units = P.vec ? (most + lanes - 1) / lanes : most;
-    const uint64_t need = std::max<uint64_t>(1, (units + mr::kThreads - 1) / mr::kThreads);
-    const int target = sm_count() * mr::kBlocksPerSm;
-    uint64_t gx = std::max(1, target / P.nseg);
-    gx = std::min(gx, need);
-    return dim3((unsigned)gx, (unsigned)P.nseg, 1);
+// Tile counts per segment (prefix sums into P.tile_start, the largest in
+// P.tiles_max) and the 1-D grid: a few CTAs per SM, never more than there are
+// tiles.
+dim3 plan_tiles(mr::ReduceParams& P, int lanes) {
+    const uint64_t per_tile = P.vec ? (uint64_t)mr::kThreads * mr::reduce_unroll(P.W) : (uint64_t)mr::kThreads;
+    P.tile_start[0] = 0;
+    P.tiles_max = 0;
+    for (int i = 0; i < P.nseg; ++i) {
+        const mr::Segment& g = P.seg[i];
+        uint64_t units = g.hi - g.lo;
+        if (P.vec) {
+            const uint64_t va = (g.lo + lanes - 1) / lanes, vb = g.hi / lanes;
+            units = va < vb ? vb - va : 0;
+        }
+        P.tile_start[i + 1] = P.tile_start[i] + (units + per_tile - 1) / per_tile;
+        P.tiles_max = std::max(P.tiles_max, P.tile_start[i + 1] - P.tile_start[i]);
+    }
+    const uint64_t vtiles = P.vec ? P.tiles_max * P.nseg : P.tile_start[P.nseg];
+    const uint64_t tiles = std::max<uint64_t>(vtiles, (uint64_t)P.nseg);
+    const int per_sm = mr::reduce_blocks_per_sm(mr::reduce_wcap(P.W));
+    const uint64_t gx = std::min<uint64_t>((uint64_t)sm_count() * per_sm, tiles);
+    return dim3((unsigned)std::max<uint64_t>(gx, 1), 1, 1);
 }
 
 cudaError_t launch_reduce(mr_dtype_t dtype, const mr::ReduceParams& P, mr_op_t op, mr_algo_t algo,
@@ -187,15 +200,15 @@ mr_status_t run_reduce(const char* what, int mode, const void* const* send, void
         vec = vec && ((uintptr_t)send[r] % vb == 0) && ((uintptr_t)recv[r] % vb == 0);
     if (mode == mr::MODE_REDUCE_SCATTER) vec = vec && ((N / W) * eb) % vb == 0;
     P.vec = vec ? 1 : 0;
-    const dim3 grid = reduce_grid(P, vb / eb);
+    const dim3 grid = plan_tiles(P, vb / eb);
     const cudaError_t err = launch_reduce(dtype, P, op, algo, grid, (cudaStream_t)stream);
     if (err != cudaSuccess)
         return fail(MR_ERR_CUDA, "%s launch failed: %s", what, cudaGetErrorString(err));
     g_launches.fetch_add(1, std::memory_order_relaxed);
     if (debug_level() > 0)
-        fprintf(stderr, "[mr] %s dtype=%s op=%s algo=%s W=%d N=%zu segments=%d vector=%d grid=%ux%u threads=%d\n",
-                what, dtype_name(dtype), op_name(op), algo_name(algo), W, N, P.nseg, P.vec, grid.x, grid.y,
-                mr::kThreads);
+        fprintf(stderr, "[mr] %s dtype=%s op=%s algo=%s W=%d N=%zu segments=%d tiles=%llu vector=%d grid=%u threads=%d\n",
+                what, dtype_name(dtype), op_name(op), algo_name(algo), W, N, P.nseg,
+                (unsigned long long)P.tile_start[P.nseg], P.vec, grid.x, mr::kThreads);
     return MR_OK;
 }
 

@@ -12,7 +12,7 @@ namespace mr {
 constexpr int kMaxRanks = MR_MAX_RANKS;
 constexpr int kMaxSegments = MR_MAX_RANKS + 1;
 constexpr int kThreads = 256;       // threads per CTA for every kernel
-constexpr int kBlocksPerSm = 2;     // resident CTAs per SM the reduce kernels are built for
+constexpr int kBlocksPerSm = 2;     // resident CTAs per SM for the all-gather and wide reductions
 
 // A run of elements with one accumulation order and one output placement:
 // a chunk of the ring, or a chunk cut at the tree-1 / tree-2 boundary.
@@ -29,6 +29,8 @@ struct ReduceParams {
     const void* in[kMaxRanks];
     void* out[kMaxRanks];
     Segment seg[kMaxSegments];
+    uint64_t tile_start[kMaxSegments + 1];   // tiles of segments [0, i) (prefix count)
+    uint64_t tiles_max;                      // most tiles of any one segment
     int W;
     int nseg;
     int mode;
@@ -46,8 +48,15 @@ struct GatherParams {
     int vec;        // 1: 16-byte vector path (pointers aligned, C*esize % 16 == 0)
 };
 
-// Vector width in bytes used by the reduce kernels for a given W.
+// The reduce kernel variant for a given W: register slots for W contributions
+// (WCAP), vector width in bytes, and vectors per thread per tile (U), chosen
+// so that each thread keeps about eight 16-byte loads in flight.
+inline int reduce_wcap(int W) { return W <= 2 ? 2 : W <= 4 ? 4 : W <= 8 ? 8 : W <= 16 ? 16 : 64; }
 inline int reduce_vector_bytes(int W) { return W <= 16 ? 16 : 4; }
+inline int reduce_unroll(int W) { return W <= 2 ? 4 : W <= 4 ? 2 : 1; }
+// Resident CTAs per SM the reduce kernel of a width class is built for (its
+// register budget allows three up to W = 8).
+constexpr int reduce_blocks_per_sm(int wcap) { return wcap <= 8 ? 3 : 2; }
 
 cudaError_t launch_reduce_fp32(const ReduceParams& P, int op, int algo, dim3 grid, cudaStream_t s);
 cudaError_t launch_reduce_bf16(const ReduceParams& P, int op, int algo, dim3 grid, cudaStream_t s);

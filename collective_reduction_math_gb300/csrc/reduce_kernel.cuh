@@ -14,12 +14,13 @@
 // Memory-bound: 2*W*N*b HBM bytes for all-reduce, (W+1)*N*b for
 // reduce-scatter, at most W-1 combines per element.  No tensor cores.
 //
-// Layout of the work: blockIdx.y picks a segment (one chunk, or a chunk cut at
-// the tree-1/tree-2 boundary), so the accumulation order is uniform across a
-// CTA.  blockIdx.x strides over the segment's aligned vectors; the unaligned
-// head and tail of a segment (fewer than one vector each), and whole segments
-// whose pointers are not vector-aligned, run the same arithmetic one element
-// per thread.
+// Layout of the work: the buffer is cut into segments (one chunk, or a chunk
+// cut at the tree-1/tree-2 boundary), each with one accumulation order, and
+// each segment into tiles of kThreads*U aligned vectors.  A 1-D grid of
+// CTAs (a few per SM) strides over the tiles, dealt round-robin across the
+// segments, so a tile's order is uniform across its CTA.  The unaligned head and tail of a segment
+// (fewer than one vector each), and whole segments whose pointers are not
+// vector-aligned, run the same arithmetic one element per thread.
 #pragma once
 
 #include <cuda_bf16.h>
@@ -202,8 +203,8 @@ __device__ __forceinline__ int order_rank(int W, const Segment& sg, int i) {
     else return tree_rank(W, sg.tree, i);
 }
 
-template <int DT, int OP, int ALGO, int WCAP, int VB>
-__global__ void __launch_bounds__(kThreads, kBlocksPerSm)
+template <int DT, int OP, int ALGO, int WCAP, int VB, int U>
+__global__ void __launch_bounds__(kThreads, reduce_blocks_per_sm(WCAP))
 reduce_kernel(const __grid_constant__ ReduceParams P) {
     using A = Arith<DT, OP>;
     using raw_t = typename A::raw_t;
@@ -211,87 +212,124 @@ reduce_kernel(const __grid_constant__ ReduceParams P) {
     constexpr int EB = Elem<DT>::kBytes;
     constexpr int LANES = VB / EB;
 
-    const Segment& sg = P.seg[blockIdx.y];
     const int W = P.W;
     const float s = P.scale;
     const bool rs = (P.mode == MODE_REDUCE_SCATTER);
 
-    // Input pointers in this segment's accumulation order: in registers for
-    // up to 16 ranks, in a shared-memory table beyond that.
+    // Input pointers in the current segment's accumulation order: in
+    // registers for up to 16 ranks, in a shared-memory table beyond that.
     constexpr bool kTable = WCAP > 16;
     __shared__ const char* table[kTable ? WCAP : 1];
     const char* src[kTable ? 1 : WCAP];
-    if constexpr (kTable) {
-        if (threadIdx.x < W)
-            table[threadIdx.x] = static_cast<const char*>(P.in[order_rank<ALGO>(W, sg, threadIdx.x)]);
-        __syncthreads();
-    } else {
+    int cur = -1;
+    auto enter = [&](int seg) {
+        if (seg == cur) return;
+        cur = seg;
+        if constexpr (kTable) {
+            __syncthreads();
+            if (threadIdx.x < W)
+                table[threadIdx.x] = static_cast<const char*>(P.in[order_rank<ALGO>(W, P.seg[seg], threadIdx.x)]);
+            __syncthreads();
+        } else {
 #pragma unroll
-        for (int i = 0; i < WCAP; ++i)
-            src[i] = (i < W) ? static_cast<const char*>(P.in[order_rank<ALGO>(W, sg, i)]) : nullptr;
-    }
+            for (int i = 0; i < WCAP; ++i)
+                src[i] = (i < W) ? static_cast<const char*>(P.in[order_rank<ALGO>(W, P.seg[seg], i)]) : nullptr;
+        }
+    };
     auto input = [&](int i) -> const char* {
         if constexpr (kTable) return table[i];
         else return src[i];
     };
 
-    const uint64_t tid = (uint64_t)blockIdx.x * kThreads + threadIdx.x;
-    const uint64_t stride = (uint64_t)gridDim.x * kThreads;
-
-    // Vector part: vectors [va, vb) lie wholly inside [lo, hi).
-    uint64_t va = 0, vb = 0;
-    if (P.vec) {
-        va = (sg.lo + LANES - 1) / LANES;
-        vb = sg.hi / LANES;
-        if (va > vb) va = vb;
-    }
-    for (uint64_t v = va + tid; v < vb; v += stride) {
-        const uint64_t off = v * VB;
-        Vec<VB> raw[WCAP];
+    // One element, reduced from scratch (heads, tails, unaligned buffers).
+    auto element = [&](const Segment& sg, uint64_t e) {
+        acc_t y[WCAP];
 #pragma unroll
         for (int i = 0; i < WCAP; ++i)
-            if (i < W) raw[i] = load_vec<VB>(input(i) + off);
-        Vec<VB> res;
-#pragma unroll
-        for (int l = 0; l < LANES; ++l) {
-            acc_t y[WCAP];
-#pragma unroll
-            for (int i = 0; i < WCAP; ++i)
-                if (i < W) y[i] = A::read(get_lane<raw_t, VB>(raw[i], l), s);
-            set_lane<raw_t, VB>(res, l, A::post(fold<A, ALGO, WCAP>(y, W), W));
-        }
+            if (i < W) y[i] = A::read(__ldg(reinterpret_cast<const raw_t*>(input(i)) + e), s);
+        const raw_t r = A::post(fold<A, ALGO, WCAP>(y, W), W);
         if (rs) {
-            store_vec<VB>(static_cast<char*>(P.out[sg.k]) + off - sg.out_lo * EB, res);
+            static_cast<raw_t*>(P.out[sg.k])[e - sg.out_lo] = r;
         } else {
 #pragma unroll
             for (int j = 0; j < WCAP; ++j)
-                if (j < W) store_vec<VB>(static_cast<char*>(P.out[j]) + off, res);
+                if (j < W) static_cast<raw_t*>(P.out[j])[e] = r;
         }
-    }
+    };
 
-    // Element part: the head [lo, va*LANES) and the tail [vb*LANES, hi), or the
-    // whole segment when the vector path is off.
-    uint64_t h0 = sg.lo, h1 = sg.hi, t0 = sg.hi, t1 = sg.hi;
-    if (P.vec && va < vb) {
-        h1 = va * LANES;
-        t0 = vb * LANES;
-    }
-#pragma unroll 1
-    for (int part = 0; part < 2; ++part) {
-        const uint64_t e0 = part ? t0 : h0, e1 = part ? t1 : h1;
-        for (uint64_t e = e0 + tid; e < e1; e += stride) {
-            acc_t y[WCAP];
+    int seg = 0;
+    if (P.vec) {
+        // Vector tiles are dealt round-robin across segments: tile t is tile
+        // t / nseg of segment t % nseg, and CTAs stride over t.  The grid's
+        // live tiles are thus spread over every chunk of every rank buffer;
+        // measured on GB300 this keeps HBM busier than sweeping the segments
+        // one after another.
+        const uint64_t ntiles = P.tiles_max * (uint64_t)P.nseg;
+        constexpr uint64_t kTile = (uint64_t)kThreads * U;    // vectors per tile
+        for (uint64_t t = blockIdx.x; t < ntiles; t += gridDim.x) {
+            seg = (int)(t % (uint64_t)P.nseg);
+            const uint64_t local = t / (uint64_t)P.nseg;
+            if (local >= P.tile_start[seg + 1] - P.tile_start[seg]) continue;
+            enter(seg);
+            const Segment& sg = P.seg[seg];
+            const uint64_t va = (sg.lo + LANES - 1) / LANES, vb = sg.hi / LANES;
+            const uint64_t v0 = va + local * kTile + threadIdx.x;
+            // U*W independent 16-byte loads in flight before the first fold.
+            Vec<VB> raw[U][WCAP];
 #pragma unroll
-            for (int i = 0; i < WCAP; ++i)
-                if (i < W) y[i] = A::read(__ldg(reinterpret_cast<const raw_t*>(input(i)) + e), s);
-            const raw_t r = A::post(fold<A, ALGO, WCAP>(y, W), W);
-            if (rs) {
-                static_cast<raw_t*>(P.out[sg.k])[e - sg.out_lo] = r;
-            } else {
+            for (int u = 0; u < U; ++u) {
+                const uint64_t v = v0 + (uint64_t)u * kThreads;
+                if (v < vb) {
 #pragma unroll
-                for (int j = 0; j < WCAP; ++j)
-                    if (j < W) static_cast<raw_t*>(P.out[j])[e] = r;
+                    for (int i = 0; i < WCAP; ++i)
+                        if (i < W) raw[u][i] = load_vec<VB>(input(i) + v * VB);
+                }
             }
+#pragma unroll
+            for (int u = 0; u < U; ++u) {
+                const uint64_t v = v0 + (uint64_t)u * kThreads;
+                if (v >= vb) break;
+                const uint64_t off = v * VB;
+                Vec<VB> res;
+#pragma unroll
+                for (int l = 0; l < LANES; ++l) {
+                    acc_t y[WCAP];
+#pragma unroll
+                    for (int i = 0; i < WCAP; ++i)
+                        if (i < W) y[i] = A::read(get_lane<raw_t, VB>(raw[u][i], l), s);
+                    set_lane<raw_t, VB>(res, l, A::post(fold<A, ALGO, WCAP>(y, W), W));
+                }
+                if (rs) {
+                    store_vec<VB>(static_cast<char*>(P.out[sg.k]) + off - sg.out_lo * EB, res);
+                } else {
+#pragma unroll
+                    for (int j = 0; j < WCAP; ++j)
+                        if (j < W) store_vec<VB>(static_cast<char*>(P.out[j]) + off, res);
+                }
+            }
+        }
+        // The elements outside whole vectors (fewer than 2*LANES per segment):
+        // segment i's are done by CTA i mod gridDim.x.
+        for (int i = blockIdx.x; i < P.nseg; i += gridDim.x) {
+            enter(i);
+            const Segment& sg = P.seg[i];
+            const uint64_t va = (sg.lo + LANES - 1) / LANES, vb = sg.hi / LANES;
+            const uint64_t h1 = va < vb ? va * LANES : sg.hi;   // head [lo, h1)
+            const uint64_t t0 = va < vb ? vb * LANES : sg.hi;   // tail [t0, hi)
+            const uint64_t nh = h1 - sg.lo, n = nh + (sg.hi - t0);
+            for (uint64_t x = threadIdx.x; x < n; x += kThreads)
+                element(sg, x < nh ? sg.lo + x : t0 + (x - nh));
+        }
+    } else {
+        // Buffers not aligned to the vector width: tiles of kThreads elements,
+        // segment after segment.
+        const uint64_t ntiles = P.tile_start[P.nseg];
+        for (uint64_t t = blockIdx.x; t < ntiles; t += gridDim.x) {
+            while (t >= P.tile_start[seg + 1]) ++seg;
+            enter(seg);
+            const Segment& sg = P.seg[seg];
+            const uint64_t e = sg.lo + (t - P.tile_start[seg]) * kThreads + threadIdx.x;
+            if (e < sg.hi) element(sg, e);
         }
     }
 }
@@ -302,9 +340,13 @@ cudaError_t launch_reduce(const ReduceParams& P, int op, int algo, dim3 grid, cu
     auto go = [&](auto op_c, auto algo_c) -> cudaError_t {
         constexpr int OP = decltype(op_c)::value;
         constexpr int ALGO = decltype(algo_c)::value;
-        if (P.W <= 8) reduce_kernel<DT, OP, ALGO, 8, 16><<<grid, kThreads, 0, stream>>>(P);
-        else if (P.W <= 16) reduce_kernel<DT, OP, ALGO, 16, 16><<<grid, kThreads, 0, stream>>>(P);
-        else reduce_kernel<DT, OP, ALGO, 64, 4><<<grid, kThreads, 0, stream>>>(P);
+        switch (reduce_wcap(P.W)) {
+            case 2: reduce_kernel<DT, OP, ALGO, 2, 16, 4><<<grid, kThreads, 0, stream>>>(P); break;
+            case 4: reduce_kernel<DT, OP, ALGO, 4, 16, 2><<<grid, kThreads, 0, stream>>>(P); break;
+            case 8: reduce_kernel<DT, OP, ALGO, 8, 16, 1><<<grid, kThreads, 0, stream>>>(P); break;
+            case 16: reduce_kernel<DT, OP, ALGO, 16, 16, 1><<<grid, kThreads, 0, stream>>>(P); break;
+            default: reduce_kernel<DT, OP, ALGO, 64, 4, 1><<<grid, kThreads, 0, stream>>>(P); break;
+        }
         return cudaGetLastError();
     };
     auto with_algo = [&](auto op_c) -> cudaError_t {
