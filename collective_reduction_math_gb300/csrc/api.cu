@@ -152,7 +152,9 @@ int plan_segments(int W, uint64_t N, mr_algo_t algo, mr::Segment* seg) {
 // P.tiles_max) and the 1-D grid: a few CTAs per SM, never more than there are
 // tiles.
 dim3 plan_tiles(mr::ReduceParams& P, int lanes) {
-    const uint64_t per_tile = P.vec ? (uint64_t)mr::kThreads * mr::reduce_unroll(P.W) : (uint64_t)mr::kThreads;
+    const bool rs = P.mode == mr::MODE_REDUCE_SCATTER;
+    const int u = mr::reduce_unroll(P.W, rs);
+    const uint64_t per_tile = P.vec ? (uint64_t)mr::kThreads * u : (uint64_t)mr::kThreads;
     P.tile_start[0] = 0;
     P.tiles_max = 0;
     for (int i = 0; i < P.nseg; ++i) {
@@ -167,7 +169,7 @@ dim3 plan_tiles(mr::ReduceParams& P, int lanes) {
     }
     const uint64_t vtiles = P.vec ? P.tiles_max * P.nseg : P.tile_start[P.nseg];
     const uint64_t tiles = std::max<uint64_t>(vtiles, (uint64_t)P.nseg);
-    const int per_sm = mr::reduce_blocks_per_sm(mr::reduce_wcap(P.W));
+    const int per_sm = mr::reduce_blocks_per_sm(mr::reduce_wcap(P.W), u);
     const uint64_t gx = std::min<uint64_t>((uint64_t)sm_count() * per_sm, tiles);
     return dim3((unsigned)std::max<uint64_t>(gx, 1), 1, 1);
 }
@@ -273,17 +275,17 @@ mr_status_t mr_all_gather(const void* const* send, void* const* recv, int W, siz
     bool vec = (C * b) % 16 == 0;
     for (int r = 0; r < W; ++r) vec = vec && ((uintptr_t)send[r] % 16 == 0) && ((uintptr_t)recv[r] % 16 == 0);
     P.vec = vec ? 1 : 0;
+    const uint64_t per_tile = vec ? (uint64_t)mr::kThreads * mr::kGatherUnroll : (uint64_t)mr::kThreads;
     const uint64_t units = vec ? (C * b) / 16 : C;
-    const uint64_t need = std::max<uint64_t>(1, (units + mr::kThreads - 1) / mr::kThreads);
-    uint64_t gx = std::max(1, sm_count() * mr::kBlocksPerSm / W);
-    gx = std::min(gx, need);
-    const dim3 grid((unsigned)gx, (unsigned)W, 1);
+    const uint64_t tiles = std::max<uint64_t>(1, (units + per_tile - 1) / per_tile) * (uint64_t)W;
+    const uint64_t gx = std::min<uint64_t>((uint64_t)sm_count() * mr::kGatherBlocksPerSm, tiles);
+    const dim3 grid((unsigned)gx, 1, 1);
     const cudaError_t err = mr::launch_all_gather(P, grid, (cudaStream_t)stream);
     if (err != cudaSuccess) return fail(MR_ERR_CUDA, "all_gather launch failed: %s", cudaGetErrorString(err));
     g_launches.fetch_add(1, std::memory_order_relaxed);
     if (debug_level() > 0)
-        fprintf(stderr, "[mr] all_gather dtype=%s W=%d N=%zu vector=%d grid=%ux%u threads=%d\n", dtype_name(dtype),
-                W, N, P.vec, grid.x, grid.y, mr::kThreads);
+        fprintf(stderr, "[mr] all_gather dtype=%s W=%d N=%zu vector=%d grid=%u threads=%d\n", dtype_name(dtype),
+                W, N, P.vec, grid.x, mr::kThreads);
     return MR_OK;
 }
 

@@ -204,7 +204,7 @@ __device__ __forceinline__ int order_rank(int W, const Segment& sg, int i) {
 }
 
 template <int DT, int OP, int ALGO, int WCAP, int VB, int U>
-__global__ void __launch_bounds__(kThreads, reduce_blocks_per_sm(WCAP))
+__global__ void __launch_bounds__(kThreads, reduce_blocks_per_sm(WCAP, U))
 reduce_kernel(const __grid_constant__ ReduceParams P) {
     using A = Arith<DT, OP>;
     using raw_t = typename A::raw_t;
@@ -340,12 +340,16 @@ cudaError_t launch_reduce(const ReduceParams& P, int op, int algo, dim3 grid, cu
     auto go = [&](auto op_c, auto algo_c) -> cudaError_t {
         constexpr int OP = decltype(op_c)::value;
         constexpr int ALGO = decltype(algo_c)::value;
+        const bool rs = P.mode == MODE_REDUCE_SCATTER;
         switch (reduce_wcap(P.W)) {
-            case 2: reduce_kernel<DT, OP, ALGO, 2, 16, 4><<<grid, kThreads, 0, stream>>>(P); break;
-            case 4: reduce_kernel<DT, OP, ALGO, 4, 16, 2><<<grid, kThreads, 0, stream>>>(P); break;
-            case 8: reduce_kernel<DT, OP, ALGO, 8, 16, 1><<<grid, kThreads, 0, stream>>>(P); break;
-            case 16: reduce_kernel<DT, OP, ALGO, 16, 16, 1><<<grid, kThreads, 0, stream>>>(P); break;
-            default: reduce_kernel<DT, OP, ALGO, 64, 4, 1><<<grid, kThreads, 0, stream>>>(P); break;
+            case 2: reduce_kernel<DT, OP, ALGO, 2, 16, reduce_unroll_for(2, false)><<<grid, kThreads, 0, stream>>>(P); break;
+            case 4: reduce_kernel<DT, OP, ALGO, 4, 16, reduce_unroll_for(4, false)><<<grid, kThreads, 0, stream>>>(P); break;
+            case 8:
+                if (rs) reduce_kernel<DT, OP, ALGO, 8, 16, reduce_unroll_for(8, true)><<<grid, kThreads, 0, stream>>>(P);
+                else reduce_kernel<DT, OP, ALGO, 8, 16, reduce_unroll_for(8, false)><<<grid, kThreads, 0, stream>>>(P);
+                break;
+            case 16: reduce_kernel<DT, OP, ALGO, 16, 16, reduce_unroll_for(16, false)><<<grid, kThreads, 0, stream>>>(P); break;
+            default: reduce_kernel<DT, OP, ALGO, 64, 4, reduce_unroll_for(64, false)><<<grid, kThreads, 0, stream>>>(P); break;
         }
         return cudaGetLastError();
     };
