@@ -17,6 +17,9 @@ What each routine follows (page title and section):
   * ``tree``: "The double binary tree".
   * ``chunk_lo``: Eq. (2), "Local shard bounds" (NCCL M2N).
   * ``bf16_rne``: the single bf16 rounding of an fp32 accumulator.
+  * ``allreduce_rmsnorm``: "How this survives ten thousand GPUs" (post on NCCL
+    all-reduce): in decoding, the merge (residual add) and the RMSNorm that
+    follow the all-reduce are fused into it.
 
 Parity unpinned: NaN and infinity payloads through min/max and bf16 rounding.
 """
@@ -172,3 +175,30 @@ def bf16_rne(bits_u32) -> np.ndarray:
     out = np.empty(a.size, np.uint16)
     lib().or_f32_to_bf16_rne_array(a.ctypes.data, out.ctypes.data, a.size)
     return out
+
+
+def allreduce_rmsnorm(dtype: str, algo: str, inputs, rows: int, hidden: int, weight, residual=None,
+                      eps: float = 1e-6, want_residual_out: bool = True):
+    """All-reduce sum of W buffers of rows*hidden elements, residual add, then
+    RMSNorm of every row scaled by ``weight``.  Returns (out, residual_out or
+    None); every rank's output is the same, so one copy is returned."""
+    W, N = len(inputs), inputs[0].size
+    if N != rows * hidden:
+        raise ValueError("inputs must hold rows*hidden elements")
+    _check_inputs(dtype, inputs, N)
+    L = lib()
+    if not hasattr(L, "_rms_typed"):
+        vp, sz, i = ctypes.c_void_p, ctypes.c_size_t, ctypes.c_int
+        L.or_allreduce_rmsnorm.argtypes = [i, i, i, sz, sz, vp, vp, vp, ctypes.c_double, vp, vp]
+        L.or_allreduce_rmsnorm.restype = i
+        L._rms_typed = True
+    out = np.empty(N, NP_DTYPE[dtype])
+    res_out = np.empty(N, NP_DTYPE[dtype]) if want_residual_out else None
+    w = np.ascontiguousarray(weight, dtype=NP_DTYPE[dtype])
+    r = None if residual is None else np.ascontiguousarray(residual, dtype=NP_DTYPE[dtype])
+    rc = L.or_allreduce_rmsnorm(DTYPES[dtype], ALGOS[algo], W, rows, hidden, _ptrs(inputs),
+                                None if r is None else r.ctypes.data, w.ctypes.data, eps,
+                                _ptrs([out] * W), None if res_out is None else res_out.ctypes.data)
+    if rc != 0:
+        raise ValueError("oracle allreduce_rmsnorm rejected its arguments")
+    return out, res_out

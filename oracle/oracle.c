@@ -8,6 +8,7 @@
 #include "oracle.h"
 
 #include <math.h>
+#include <stdlib.h>
 #include <string.h>
 
 /* ------------------------------------------------------------------------- */
@@ -336,5 +337,61 @@ int or_reduce_one(int dtype, int op, int algo, int W, size_t N, size_t e,
     for (int r = 0; r < W; r++) y[r] = read_contribution(dtype, op, P.s, y_raw, (size_t)r);
     acc_t acc = reduce_position(&P, k, e, y);
     store_result(dtype, op, W, acc, res, 0);
+    return 0;
+}
+
+/* ------------------------------------------------------------------------- */
+/* All-reduce with a residual add and RMSNorm after the sum                  */
+/* ("How this survives ten thousand GPUs", post on NCCL all-reduce: in       */
+/* decoding, the merge and the RMSNorm that follow the all-reduce are fused  */
+/* into it)                                                                  */
+/* ------------------------------------------------------------------------- */
+
+/* The buffer is `rows` rows of `hidden` elements.  For each element the W
+ * contributions are summed exactly as or_allreduce sums them (same chunks,
+ * same order, fp32), then the residual is added in fp32:
+ *     h = s + residual.
+ * residual_out (if non-NULL) receives h rounded to the element type.  Each
+ * row is then normalised by its root mean square and scaled by the weight:
+ *     out = h / sqrt(mean(h^2) + eps) * weight,
+ * evaluated in fp64 from the fp32 h (the exact reference the fp32 kernel is
+ * held to within a derived tolerance) and rounded once to the element type;
+ * every out[j] receives it.  fp32 and bf16 only. */
+int or_allreduce_rmsnorm(int dtype, int algo, int W, size_t rows, size_t hidden,
+                         const void* const* in, const void* residual, const void* weight, double eps,
+                         void* const* out, void* residual_out) {
+    plan_t P;
+    size_t N = rows * hidden;
+    if (dtype == OR_INT32) return -1;
+    if (make_plan(&P, dtype, OR_SUM, algo, W, N) != 0) return -1;
+    if (hidden == 0 || !weight) return -1;
+    float* h = (float*)malloc(sizeof(float) * (hidden ? hidden : 1));
+    if (!h) return -1;
+    for (size_t row = 0; row < rows; row++) {
+        double ss = 0.0;
+        for (size_t i = 0; i < hidden; i++) {
+            size_t e = row * hidden + i;
+            int k = 0;
+            while (or_chunk_lo(W, N, k + 1) <= e) k++;
+            acc_t s = reduce_from_buffers(&P, k, e, in);
+            float hv = s.f;
+            if (residual) hv = hv + widen(dtype, residual, e).f;
+            h[i] = hv;
+            if (residual_out) {
+                acc_t a;
+                a.f = hv;
+                store_result(dtype, OR_SUM, W, a, residual_out, e);
+            }
+            ss += (double)hv * (double)hv;
+        }
+        double inv = 1.0 / sqrt(ss / (double)hidden + eps);
+        for (size_t i = 0; i < hidden; i++) {
+            size_t e = row * hidden + i;
+            acc_t a;
+            a.f = (float)((double)h[i] * inv * (double)widen(dtype, weight, i).f);
+            for (int j = 0; j < W; j++) store_result(dtype, OR_SUM, W, a, out[j], e);
+        }
+    }
+    free(h);
     return 0;
 }

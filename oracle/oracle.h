@@ -83,6 +83,14 @@ int or_all_gather(int dtype, int W, size_t N,
 int or_reduce_one(int dtype, int op, int algo, int W, size_t N, size_t e,
                   const void* y, void* res);
 
+/* All-reduce (sum) of `rows` x `hidden` elements, then h = sum + residual
+ * (residual may be NULL) and out[j] = RMSNorm(h) * weight for every j;
+ * residual_out (may be NULL) receives h.  fp32 / bf16 only.  The norm is
+ * evaluated in fp64 from the fp32 h. */
+int or_allreduce_rmsnorm(int dtype, int algo, int W, size_t rows, size_t hidden,
+                         const void* const* in, const void* residual, const void* weight, double eps,
+                         void* const* out, void* residual_out);
+
 #ifdef __cplusplus
 }
 #endif
