@@ -35,6 +35,8 @@ METRIC = "fused all-reduce algo GB/s and % of GB300 HBM roofline vs message size
 WORKLOAD = "ddp_bucket_fp32_w8"
 FALLBACK_HBM_GBS = 6800.0
 L2_BYTES = 129 * 1000 * 1000
+GRAPH_BELOW_BYTES = 256 << 20     # steps moving less than this are timed as CUDA-graph replays
+GRAPH_STEPS = 50
 KERNEL_SOURCES = ["reduce_kernel.cuh", "order.cuh", "mr_internal.h", "reduce_fp32.cu", "api.cu"]
 PROFILE = os.path.join(ROOT, "profiles", "reduce_kernel_ddp_bucket_fp32_w8.txt")
 
@@ -49,7 +51,8 @@ def parse_args():
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--e2e-steps", type=int, default=20)
     p.add_argument("--workload", default=WORKLOAD, help="a workload of synth.WORKLOADS (default: the headline)")
-    p.add_argument("--collective", choices=["allreduce", "reduce_scatter", "all_gather"], default=None,
+    p.add_argument("--collective", choices=["allreduce", "reduce_scatter", "all_gather", "allreduce_rmsnorm"],
+                   default=None,
                    help="the collective timed as one step (default: the workload's own)")
     p.add_argument("--op", default=None)
     p.add_argument("--algo", default="ring")
@@ -353,7 +356,8 @@ class Step:
 
     DEFAULTS = {"small_int_fp32_w2": ("allreduce", "sum"), "ddp_bucket_fp32_w8": ("allreduce", "avg"),
                 "fsdp_bf16_w8": ("reduce_scatter", "avg"), "int_counts_w16": ("allreduce", "sum"),
-                "sweep_fp32_w8": ("allreduce", "sum")}
+                "sweep_fp32_w8": ("allreduce", "sum"), "tp_decode_rmsnorm_bf16_w8": ("allreduce_rmsnorm", "sum"),
+                "tp_prefill_rmsnorm_bf16_w8": ("allreduce_rmsnorm", "sum")}
 
     def __init__(self, args, mr, torch, dev):
         import numpy as np
@@ -374,6 +378,20 @@ class Step:
         def dev_t(h):
             return torch.from_numpy(h.view(np.int16) if self.dtype == "bf16" else h).to(dev).view(tdt)
 
+        if self.collective == "allreduce_rmsnorm":
+            ins, res, wt = synth.workload_norm_operands(self.workload)
+            self.host_in = ins + [res, wt]
+            self.xs = [dev_t(h) for h in ins]
+            self.res, self.wt = dev_t(res), dev_t(wt)
+            self.ys = [torch.empty_like(x) for x in self.xs] + [torch.empty_like(self.res)]
+            H = w["hidden"]
+            self.bytes = (2 * W + 2) * N * b + H * b
+            self.call = lambda: mr.mr_allreduce_rmsnorm(self.xs, self.ys[:W], self.wt, residual=self.res,
+                                                        residual_out=self.ys[W], eps=1e-6, algo=self.algo)
+            self.in_bytes = sum(x.numel() * b for x in self.xs) + self.res.numel() * b + H * b
+            self.out_bytes = sum(y.numel() * b for y in self.ys)
+            self.e2e_in = self.xs + [self.res, self.wt]
+            return
         if self.collective == "all_gather":
             self.host_in = synth.workload_param_shards(self.workload, N=N) if "param_dist" in w else \
                 [h[:C].copy() for h in synth.workload_inputs(self.workload, N=N)]
@@ -394,10 +412,12 @@ class Step:
                 self.call = lambda: mr.mr_reduce_scatter(self.xs, self.ys, op=self.op, algo=self.algo)
         self.in_bytes = sum(x.numel() * b for x in self.xs)
         self.out_bytes = sum(y.numel() * b for y in self.ys)
+        self.e2e_in = self.xs
 
     def config(self):
         kernel = {"allreduce": "fused all-reduce", "reduce_scatter": "reduce-scatter",
-                  "all_gather": "all-gather"}[self.collective]
+                  "all_gather": "all-gather",
+                  "allreduce_rmsnorm": "fused all-reduce + residual + RMSNorm"}[self.collective]
         l2 = ("inputs larger than L2, no flush" if self.in_bytes + self.out_bytes > 4 * L2_BYTES
               else "working set within 4x L2: warm-cache figure")
         return {"workload": self.workload, "collective": self.collective, "kernel": kernel, "W": self.W,
@@ -438,14 +458,37 @@ def run_mine(args):
     if dist:
         dist.barrier()
 
+    # Small steps are launch-bound from Python: time them as replays of a CUDA
+    # graph holding kGraph consecutive steps, so the events see device time.
+    use_graph = S.bytes < GRAPH_BELOW_BYTES
+    timed_step = step
+    per_replay = 1
+    if use_graph:
+        g = torch.cuda.CUDAGraph()
+        side = torch.cuda.Stream()
+        side.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(side):
+            step()
+        torch.cuda.current_stream().wait_stream(side)
+        with torch.cuda.graph(g):
+            for _ in range(GRAPH_STEPS):
+                step()
+        torch.cuda.synchronize()
+        timed_step = g.replay
+        per_replay = GRAPH_STEPS
+        for _ in range(3):
+            g.replay()
+        torch.cuda.synchronize()
+
     gpu_index = local
     vis = os.environ.get("CUDA_VISIBLE_DEVICES", "")
     if vis and vis.split(",")[0].strip().isdigit():
         gpu_index = int(vis.split(",")[local].strip())
     sampler = ClockSampler(gpu_index)
     sampler.start()
-    K = args.steps
-    per = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
+    K = max(per_replay, (args.steps // per_replay) * per_replay)
+    per = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(K // per_replay)]
     t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     torch.cuda.synchronize()
     if dist:
@@ -455,17 +498,18 @@ def run_mine(args):
     t_start.record()
     for a, b in per:
         a.record()
-        step()
+        timed_step()
         b.record()
     t_end.record()
     torch.cuda.synchronize()
     sampler.mark(False)
     if dist:
         dist.barrier()
-    launches = mr.mr_launch_count() - launches0
+    # a graph replay launches its captured kernels without calling the library
+    launches = (mr.mr_launch_count() - launches0) if not use_graph else K
     clocks = sampler.stop()
     total_ms = t_start.elapsed_time(t_end)
-    kern_ms = statistics.mean(a.elapsed_time(b) for a, b in per)
+    kern_ms = statistics.mean(a.elapsed_time(b) for a, b in per) / per_replay
     if dist:
         t = torch.tensor([total_ms], device=dev)
         dist.all_reduce(t, op=dist.ReduceOp.MAX)
@@ -487,7 +531,7 @@ def run_mine(args):
         hout = [torch.empty(y.numel() * y.element_size(), dtype=torch.uint8).pin_memory() for y in ys]
 
         def e2e_step():
-            for x, h in zip(xs, hin):
+            for x, h in zip(S.e2e_in, hin):
                 x.view(torch.uint8).copy_(h, non_blocking=True)
             step()
             for h, y in zip(hout, ys):
@@ -532,7 +576,9 @@ def run_mine(args):
             "warmup": max(3, args.warmup), "ms_per_step": total_ms / K, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f32" if S.dtype != "int32" else "i32",
             "data": "synthetic",
-            "config": S.config(), "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
+            "config": dict(S.config(), timing=(f"CUDA graph of {GRAPH_STEPS} steps per replay" if use_graph
+                                               else "one library call per step")),
+            "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
             "gpu_launches": launches, "clocks": clocks, "device": torch.cuda.get_device_name(dev),
             "extras": extra,
         }

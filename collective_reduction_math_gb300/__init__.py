@@ -17,7 +17,8 @@ import ctypes
 import os
 
 __all__ = [
-    "mr_allreduce", "mr_reduce_scatter", "mr_all_gather", "mr_status_string", "mr_last_error",
+    "mr_allreduce", "mr_reduce_scatter", "mr_all_gather", "mr_allreduce_rmsnorm", "mr_status_string",
+    "mr_last_error",
     "mr_allreduce_ptrs", "mr_plan_ring_order", "mr_plan_tree", "mr_chunk_lo", "mr_launch_count", "MRError",
     "load", "LIB_PATH",
     "DTYPES", "OPS", "ALGOS", "MAX_RANKS",
@@ -57,6 +58,8 @@ def load():
     L.mr_reduce_scatter.restype = i
     L.mr_all_gather.argtypes = [vp, vp, i, sz, i, vp]
     L.mr_all_gather.restype = i
+    L.mr_allreduce_rmsnorm.argtypes = [vp, vp, i, sz, sz, vp, vp, vp, ctypes.c_float, i, i, vp]
+    L.mr_allreduce_rmsnorm.restype = i
     L.mr_status_string.argtypes = [i]
     L.mr_status_string.restype = ctypes.c_char_p
     L.mr_last_error.argtypes = []
@@ -154,6 +157,27 @@ def mr_all_gather(send, recv, stream=None):
     L = load()
     st = L.mr_all_gather(_pointers(send), _pointers(recv), len(send), recv[0].numel(), _dtype_code(recv[0]),
                          _stream(stream))
+    if st:
+        _raise(st)
+
+
+def mr_allreduce_rmsnorm(send, recv, weight, residual=None, residual_out=None, eps=1e-6, algo="ring",
+                         stream=None):
+    """All-reduce (sum) of send[0..W-1], residual add, then RMSNorm of every
+    row of ``weight.numel()`` elements scaled by ``weight``; every recv[j]
+    receives the normalised rows and residual_out (if given) the pre-norm sum
+    plus residual."""
+    _check(send, "send")
+    _check(recv, "recv")
+    L = load()
+    hidden = weight.numel()
+    n = send[0].numel()
+    if hidden == 0 or n % hidden:
+        raise ValueError("the buffers must hold whole rows of weight.numel() elements")
+    ptr = lambda t: None if t is None else t.data_ptr()  # noqa: E731
+    st = L.mr_allreduce_rmsnorm(_pointers(send), _pointers(recv), len(send), n // hidden, hidden, ptr(residual),
+                                ptr(residual_out), weight.data_ptr(), float(eps), _dtype_code(send[0]),
+                                _code(ALGOS, algo, "algo"), _stream(stream))
     if st:
         _raise(st)
 

@@ -6,6 +6,8 @@
 #include <stdio.h>
 #include <stdlib.h>
 
+#include <math.h>
+
 #include <algorithm>
 #include <atomic>
 #include <string>
@@ -91,27 +93,26 @@ mr_status_t check_op_algo(mr_op_t op, mr_algo_t algo) {
     return MR_OK;
 }
 
-// Overlap check over the 2W byte ranges.  Ranges of rank r's send and recv
-// buffers may overlap only when `inplace(r)` holds; every other pair of
-// non-empty ranges must be disjoint.  Sort by start, then sweep with the set of
-// ranges still open (which stays tiny when the buffers are disjoint).
+// Overlap check over byte ranges.  Two ranges may overlap only when
+// `allowed(a, b)` says so (an in-place form); every other pair of non-empty
+// ranges must be disjoint.  Sort by start, then sweep with the set of ranges
+// still open (which stays tiny when the buffers are disjoint).
+enum RangeKind { SEND = 0, RECV = 1, RESIDUAL = 2, RESIDUAL_OUT = 3, WEIGHT = 4 };
+const char* kind_name(int k) {
+    static const char* n[] = {"send", "recv", "residual", "residual_out", "weight"};
+    return n[k];
+}
+
 struct Range {
     uintptr_t lo, hi;
     int rank;
-    int is_recv;
+    int kind;
 };
 
-template <class InPlace>
-mr_status_t check_alias(const void* const* send, size_t send_bytes, void* const* recv, size_t recv_bytes,
-                        int W, InPlace inplace) {
-    Range rs[2 * MR_MAX_RANKS];
-    int n = 0;
-    for (int r = 0; r < W; ++r) {
-        if (send_bytes) rs[n++] = {(uintptr_t)send[r], (uintptr_t)send[r] + send_bytes, r, 0};
-        if (recv_bytes) rs[n++] = {(uintptr_t)recv[r], (uintptr_t)recv[r] + recv_bytes, r, 1};
-    }
+template <class Allowed>
+mr_status_t check_overlaps(Range* rs, int n, Allowed allowed) {
     std::sort(rs, rs + n, [](const Range& a, const Range& b) { return a.lo < b.lo; });
-    int open[2 * MR_MAX_RANKS];
+    int open[2 * MR_MAX_RANKS + 8];
     int nopen = 0;
     for (int i = 0; i < n; ++i) {
         int keep = 0;
@@ -119,15 +120,30 @@ mr_status_t check_alias(const void* const* send, size_t send_bytes, void* const*
             const Range& o = rs[open[j]];
             if (o.hi <= rs[i].lo) continue;        // closed before this one starts
             open[keep++] = open[j];
-            const bool pair = o.rank == rs[i].rank && o.is_recv != rs[i].is_recv;
-            if (!(pair && inplace(o.rank)))
-                return fail(MR_ERR_ALIAS, "%s[%d] overlaps %s[%d] in a form that is not the allowed in-place one",
-                            o.is_recv ? "recv" : "send", o.rank, rs[i].is_recv ? "recv" : "send", rs[i].rank);
+            if (!allowed(o, rs[i]) && !allowed(rs[i], o))
+                return fail(MR_ERR_ALIAS, "%s[%d] overlaps %s[%d] in a form that is not an allowed in-place one",
+                            kind_name(o.kind), o.rank, kind_name(rs[i].kind), rs[i].rank);
         }
         nopen = keep;
         open[nopen++] = i;
     }
     return MR_OK;
+}
+
+// The send/recv ranges of the collectives: rank r's pair may overlap only
+// when `inplace(r)` holds.
+template <class InPlace>
+mr_status_t check_alias(const void* const* send, size_t send_bytes, void* const* recv, size_t recv_bytes,
+                        int W, InPlace inplace) {
+    Range rs[2 * MR_MAX_RANKS];
+    int n = 0;
+    for (int r = 0; r < W; ++r) {
+        if (send_bytes) rs[n++] = {(uintptr_t)send[r], (uintptr_t)send[r] + send_bytes, r, SEND};
+        if (recv_bytes) rs[n++] = {(uintptr_t)recv[r], (uintptr_t)recv[r] + recv_bytes, r, RECV};
+    }
+    return check_overlaps(rs, n, [&](const Range& a, const Range& b) {
+        return a.kind == SEND && b.kind == RECV && a.rank == b.rank && inplace(a.rank);
+    });
 }
 
 // Segments of [0, N): each chunk k = [floor(kN/W), floor((k+1)N/W)), cut at
@@ -286,6 +302,86 @@ mr_status_t mr_all_gather(const void* const* send, void* const* recv, int W, siz
     if (debug_level() > 0)
         fprintf(stderr, "[mr] all_gather dtype=%s W=%d N=%zu vector=%d grid=%u threads=%d\n", dtype_name(dtype),
                 W, N, P.vec, grid.x, mr::kThreads);
+    return MR_OK;
+}
+
+mr_status_t mr_allreduce_rmsnorm(const void* const* send, void* const* recv, int W, size_t rows, size_t hidden,
+                                 const void* residual, void* residual_out, const void* weight, float eps,
+                                 mr_dtype_t dtype, mr_algo_t algo, void* stream) {
+    g_last_error.clear();
+    mr_status_t st = check_common(send, recv, W, dtype);
+    if (st == MR_OK) st = check_op_algo(MR_SUM, algo);
+    if (st != MR_OK) return st;
+    if (dtype == MR_INT32) return fail(MR_ERR_UNSUPPORTED, "allreduce_rmsnorm takes fp32 or bf16, not int32");
+    if (hidden < 1 || hidden > mr::kMaxNormHidden)
+        return fail(MR_ERR_INVALID_ARGUMENT, "hidden = %zu is outside [1, %llu]", hidden,
+                    (unsigned long long)mr::kMaxNormHidden);
+    if (!(eps >= 0.0f) || eps == INFINITY)
+        return fail(MR_ERR_INVALID_ARGUMENT, "eps must be finite and >= 0");
+    if (rows > (SIZE_MAX / 4) / hidden) return fail(MR_ERR_INVALID_ARGUMENT, "rows * hidden overflows");
+    if (rows == 0) return MR_OK;
+    if ((st = check_pointers(send, recv, W, dtype)) != MR_OK) return st;
+    const uintptr_t a = elem_bytes(dtype) - 1;
+    if (!weight) return fail(MR_ERR_INVALID_ARGUMENT, "weight is NULL");
+    if (((uintptr_t)weight & a) || ((uintptr_t)residual & a) || ((uintptr_t)residual_out & a))
+        return fail(MR_ERR_INVALID_ARGUMENT, "weight, residual or residual_out is not aligned to its element");
+    const size_t N = rows * hidden, b = elem_bytes(dtype), bytes = N * b;
+
+    Range rs[2 * MR_MAX_RANKS + 3];
+    int n = 0;
+    for (int r = 0; r < W; ++r) {
+        rs[n++] = {(uintptr_t)send[r], (uintptr_t)send[r] + bytes, r, SEND};
+        rs[n++] = {(uintptr_t)recv[r], (uintptr_t)recv[r] + bytes, r, RECV};
+    }
+    if (residual) rs[n++] = {(uintptr_t)residual, (uintptr_t)residual + bytes, 0, RESIDUAL};
+    if (residual_out) rs[n++] = {(uintptr_t)residual_out, (uintptr_t)residual_out + bytes, 0, RESIDUAL_OUT};
+    rs[n++] = {(uintptr_t)weight, (uintptr_t)weight + hidden * b, 0, WEIGHT};
+    st = check_overlaps(rs, n, [](const Range& x, const Range& y) {
+        const bool same = x.lo == y.lo && x.hi == y.hi;
+        return same && ((x.kind == SEND && y.kind == RECV && x.rank == y.rank) ||
+                        (x.kind == RESIDUAL && y.kind == RESIDUAL_OUT));
+    });
+    if (st != MR_OK) return st;
+
+    mr::NormParams P;
+    for (int r = 0; r < W; ++r) {
+        P.in[r] = send[r];
+        P.out[r] = recv[r];
+    }
+    P.residual = residual;
+    P.residual_out = residual_out;
+    P.weight = weight;
+    P.rows = rows;
+    P.hidden = hidden;
+    P.W = W;
+    P.eps = eps;
+    P.nseg = plan_segments(W, N, algo, P.seg);
+    const int vb = mr::reduce_vector_bytes(W);
+    const size_t lanes = vb / b;
+    bool vec = hidden % lanes == 0;
+    for (int r = 0; r < W; ++r) vec = vec && ((uintptr_t)send[r] % vb == 0) && ((uintptr_t)recv[r] % vb == 0);
+    vec = vec && ((uintptr_t)weight % vb == 0) && ((uintptr_t)residual % vb == 0) && ((uintptr_t)residual_out % vb == 0);
+    P.vec = vec ? 1 : 0;
+    // A cluster of csize CTAs per row at a time; each CTA keeps its slice of
+    // the row's fp32 values in shared memory.  Few rows (decode): spread each
+    // row over up to 8 SMs, as long as every CTA keeps at least one vector
+    // per thread.
+    const size_t sms = (size_t)sm_count();
+    int csize = 1;
+    while (csize < 8 && rows * (size_t)(csize * 2) <= 2 * sms && hidden / lanes / (size_t)(csize * 2) >= mr::kThreads)
+        csize *= 2;
+    P.csize = csize;
+    const size_t slice = (hidden + csize - 1) / csize + lanes;
+    const size_t smem = ((slice * 4 + 15) / 16) * 16;
+    const size_t per_sm = std::max<size_t>(1, std::min<size_t>(8, (200 * 1024) / (smem + 1024)));
+    const size_t clusters = std::min<size_t>(rows, std::max<size_t>(1, sms * per_sm / csize));
+    const dim3 grid((unsigned)(clusters * csize), 1, 1);
+    const cudaError_t err = mr::launch_allreduce_rmsnorm(P, dtype, algo, grid, smem, (cudaStream_t)stream);
+    if (err != cudaSuccess) return fail(MR_ERR_CUDA, "allreduce_rmsnorm launch failed: %s", cudaGetErrorString(err));
+    g_launches.fetch_add(1, std::memory_order_relaxed);
+    if (debug_level() > 0)
+        fprintf(stderr, "[mr] allreduce_rmsnorm dtype=%s algo=%s W=%d rows=%zu hidden=%zu vector=%d grid=%u "
+                "cluster=%d smem=%zu\n", dtype_name(dtype), algo_name(algo), W, rows, hidden, P.vec, grid.x, csize, smem);
     return MR_OK;
 }
 

@@ -40,6 +40,25 @@ struct ReduceParams {
     float scale;    // fl32(1/W): the float avg pre-scale
 };
 
+// All-reduce + residual + RMSNorm (rows x hidden elements).
+struct NormParams {
+    const void* in[kMaxRanks];
+    void* out[kMaxRanks];
+    const void* residual;       // may be null
+    void* residual_out;         // may be null
+    const void* weight;         // hidden elements
+    Segment seg[kMaxSegments];
+    uint64_t rows, hidden;
+    int W;
+    int nseg;
+    int vec;                    // 1: 16-byte (or the width's) vectors: pointers aligned, hidden % lanes == 0
+    int csize;                  // CTAs per cluster; each takes a slice of a row's columns
+    float eps;
+};
+
+// Largest row the fused RMSNorm keeps in shared memory (fp32 per element).
+constexpr uint64_t kMaxNormHidden = 49152;
+
 struct GatherParams {
     const void* in[kMaxRanks];
     void* out[kMaxRanks];
@@ -67,5 +86,6 @@ cudaError_t launch_reduce_fp32(const ReduceParams& P, int op, int algo, dim3 gri
 cudaError_t launch_reduce_bf16(const ReduceParams& P, int op, int algo, dim3 grid, cudaStream_t s);
 cudaError_t launch_reduce_int32(const ReduceParams& P, int op, int algo, dim3 grid, cudaStream_t s);
 cudaError_t launch_all_gather(const GatherParams& P, dim3 grid, cudaStream_t s);
+cudaError_t launch_allreduce_rmsnorm(const NormParams& P, int dtype, int algo, dim3 grid, size_t smem, cudaStream_t s);
 
 }  // namespace mr

@@ -1,0 +1,254 @@
+// rmsnorm_kernel.cu -- all-reduce with the residual add and RMSNorm fused
+// after the sum: "in decoding, the merge and the RMSNorm that follow are fused
+// into the preceding all-reduce, so the collective absorbs a kernel" (post on
+// NCCL all-reduce, "How this survives ten thousand GPUs").
+//
+// The buffer is rows x hidden.  A thread-block cluster of C CTAs owns a row at
+// a time (a persistent grid of clusters strides over the rows); CTA c of the
+// cluster takes the c-th slice of the row's columns.  With few rows (decode)
+// C > 1 spreads one row over several SMs; with many rows C = 1.
+//   pass 1  for every element: reduce the W contributions exactly as the
+//           all-reduce kernel does (same chunks, same ring or tree order,
+//           fp32), add the residual (one fp32 add), write the rounded h to
+//           residual_out, keep the fp32 h in shared memory, and accumulate
+//           h*h into a per-thread fp32 partial (increasing element order);
+//   reduce  the partials with a fixed tree (warp shuffles, then the warp
+//           totals), then the C slice totals in cluster-rank order, read
+//           from each CTA's shared memory over the cluster (DSMEM), so every
+//           CTA -- and every run -- gets the same value;
+//           inv = 1 / sqrt(ss / hidden + eps), each step one IEEE operation;
+//   pass 2  out = (h * inv) * weight, rounded once, stored to all W outputs.
+// Bytes per row: W reads and W writes of the row, plus the residual read,
+// residual_out write and weight read (the weight stays in L2 across rows).
+#include <cooperative_groups.h>
+#include <cuda_runtime.h>
+
+#include "reduce_kernel.cuh"
+
+namespace cg = cooperative_groups;
+
+namespace mr {
+
+template <int DT, int ALGO, int WCAP, int VB>
+__global__ void __launch_bounds__(kThreads)
+allreduce_rmsnorm_kernel(const __grid_constant__ NormParams P) {
+    using A = Arith<DT, MR_SUM>;
+    using raw_t = typename A::raw_t;
+    constexpr int EB = Elem<DT>::kBytes;
+    constexpr int LANES = VB / EB;
+    static_assert(LANES % 4 == 0 || VB < 16, "vector lanes are moved to shared memory as float4");
+
+    extern __shared__ float4 row_smem[];
+    float* hs = reinterpret_cast<float*>(row_smem);      // this CTA's slice of the row's fp32 h
+    __shared__ float warp_part[kThreads / 32];
+    __shared__ float slice_total[2];                     // read by the cluster's peers, by row parity
+    __shared__ float inv_shared;
+
+    const int W = P.W;
+    const uint64_t H = P.hidden;
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    cg::cluster_group cluster = cg::this_cluster();
+    const int C = P.csize;
+    const int crank = (int)cluster.block_rank();
+    const uint64_t first_row = blockIdx.x / C, row_stride = gridDim.x / C;
+    // This CTA's columns: vectors [v_lo, v_hi) (vector path) or elements
+    // [c_lo, c_hi) (element path).
+    const uint64_t nv_all = H / LANES;
+    const uint64_t v_lo = nv_all * crank / C, v_hi = nv_all * (crank + 1) / C;
+    const uint64_t c_lo = H * crank / C, c_hi = H * (crank + 1) / C;
+
+    auto input = [&](const Segment& sg, int i) -> const char* {
+        return static_cast<const char*>(P.in[order_rank<ALGO>(W, sg, i)]);
+    };
+    auto segment_at = [&](uint64_t e, int from) {
+        int s = from;
+        while (e >= P.seg[s].hi) ++s;
+        return s;
+    };
+    // One element of pass 1: returns h and writes residual_out.
+    auto element_h = [&](uint64_t e, int sgi) -> float {
+        const Segment& sg = P.seg[sgi];
+        float y[WCAP];
+#pragma unroll
+        for (int i = 0; i < WCAP; ++i)
+            if (i < W) y[i] = A::read(__ldg(reinterpret_cast<const raw_t*>(input(sg, i)) + e), 0.0f);
+        float h = fold<A, ALGO, WCAP>(y, W);
+        if (P.residual) h = __fadd_rn(h, A::read(__ldg(static_cast<const raw_t*>(P.residual) + e), 0.0f));
+        if (P.residual_out) static_cast<raw_t*>(P.residual_out)[e] = A::post(h, W);
+        return h;
+    };
+
+    int parity = 0;
+    for (uint64_t row = first_row; row < P.rows; row += row_stride, parity ^= 1) {
+        const uint64_t base = row * H;
+        int sgi = segment_at(base + (P.vec ? v_lo * LANES : c_lo), 0);
+        float ss = 0.0f;
+
+        // ---- pass 1 -------------------------------------------------------
+        if (P.vec) {
+            for (uint64_t v = v_lo + threadIdx.x; v < v_hi; v += kThreads) {
+                const uint64_t e0 = base + v * LANES;
+                const uint64_t sv = v - v_lo;      // slot in this CTA's slice
+                sgi = segment_at(e0, sgi);
+                float hv[LANES];
+                if (e0 + LANES <= P.seg[sgi].hi) {
+                    const Segment& sg = P.seg[sgi];
+                    Vec<VB> raw[WCAP];
+#pragma unroll
+                    for (int i = 0; i < WCAP; ++i)
+                        if (i < W) raw[i] = load_vec<VB>(input(sg, i) + e0 * EB);
+                    Vec<VB> rv;
+                    if (P.residual) rv = load_vec<VB>(static_cast<const char*>(P.residual) + e0 * EB);
+                    Vec<VB> ro;
+#pragma unroll
+                    for (int l = 0; l < LANES; ++l) {
+                        float y[WCAP];
+#pragma unroll
+                        for (int i = 0; i < WCAP; ++i)
+                            if (i < W) y[i] = A::read(get_lane<raw_t, VB>(raw[i], l), 0.0f);
+                        float h = fold<A, ALGO, WCAP>(y, W);
+                        if (P.residual) h = __fadd_rn(h, A::read(get_lane<raw_t, VB>(rv, l), 0.0f));
+                        hv[l] = h;
+                        set_lane<raw_t, VB>(ro, l, A::post(h, W));
+                    }
+                    if (P.residual_out) store_vec<VB>(static_cast<char*>(P.residual_out) + e0 * EB, ro);
+                } else {
+                    // the vector straddles a chunk (or tree) boundary
+#pragma unroll
+                    for (int l = 0; l < LANES; ++l) hv[l] = element_h(e0 + l, segment_at(e0 + l, sgi));
+                }
+#pragma unroll
+                for (int l = 0; l < LANES; ++l) ss = __fadd_rn(ss, __fmul_rn(hv[l], hv[l]));
+                if constexpr (LANES % 4 == 0) {
+#pragma unroll
+                    for (int q = 0; q < LANES / 4; ++q)
+                        row_smem[sv * (LANES / 4) + q] = make_float4(hv[4 * q], hv[4 * q + 1], hv[4 * q + 2], hv[4 * q + 3]);
+                } else {
+#pragma unroll
+                    for (int l = 0; l < LANES; ++l) hs[sv * LANES + l] = hv[l];
+                }
+            }
+        } else {
+            for (uint64_t i = c_lo + threadIdx.x; i < c_hi; i += kThreads) {
+                const uint64_t e = base + i;
+                sgi = segment_at(e, sgi);
+                const float h = element_h(e, sgi);
+                hs[i - c_lo] = h;
+                ss = __fadd_rn(ss, __fmul_rn(h, h));
+            }
+        }
+
+        // ---- the row's sum of squares, in a fixed tree ---------------------
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) ss = __fadd_rn(ss, __shfl_down_sync(0xffffffffu, ss, o));
+        if (lane == 0) warp_part[warp] = ss;
+        __syncthreads();
+        if (warp == 0) {
+            float t = lane < kThreads / 32 ? warp_part[lane] : 0.0f;
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) t = __fadd_rn(t, __shfl_down_sync(0xffffffffu, t, o));
+            if (lane == 0) {
+                if (C == 1) inv_shared = __fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(__fdiv_rn(t, (float)H), P.eps)));
+                else slice_total[parity] = t;
+            }
+        }
+        if (C > 1) {
+            // Every CTA of the cluster adds the C slice totals in rank order.
+            // The totals alternate between two slots by row parity, so one
+            // cluster barrier per row keeps a fast CTA from overwriting a slot
+            // a peer is still reading.
+            cluster.sync();
+            if (threadIdx.x == 0) {
+                float t = 0.0f;
+                for (int r = 0; r < C; ++r) t = __fadd_rn(t, *cluster.map_shared_rank(&slice_total[parity], r));
+                inv_shared = __fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(__fdiv_rn(t, (float)H), P.eps)));
+            }
+        }
+        __syncthreads();
+        const float inv = inv_shared;
+
+        // ---- pass 2 -------------------------------------------------------
+        if (P.vec) {
+            for (uint64_t v = v_lo + threadIdx.x; v < v_hi; v += kThreads) {
+                const uint64_t sv = v - v_lo;
+                float hv[LANES];
+                if constexpr (LANES % 4 == 0) {
+#pragma unroll
+                    for (int q = 0; q < LANES / 4; ++q) {
+                        const float4 f = row_smem[sv * (LANES / 4) + q];
+                        hv[4 * q] = f.x;
+                        hv[4 * q + 1] = f.y;
+                        hv[4 * q + 2] = f.z;
+                        hv[4 * q + 3] = f.w;
+                    }
+                } else {
+#pragma unroll
+                    for (int l = 0; l < LANES; ++l) hv[l] = hs[sv * LANES + l];
+                }
+                const Vec<VB> wv = load_vec<VB>(static_cast<const char*>(P.weight) + v * VB);
+                Vec<VB> o;
+#pragma unroll
+                for (int l = 0; l < LANES; ++l)
+                    set_lane<raw_t, VB>(o, l, A::post(__fmul_rn(__fmul_rn(hv[l], inv),
+                                                                A::read(get_lane<raw_t, VB>(wv, l), 0.0f)), W));
+                const uint64_t off = (base + v * LANES) * EB;
+#pragma unroll
+                for (int j = 0; j < WCAP; ++j)
+                    if (j < W) store_vec<VB>(static_cast<char*>(P.out[j]) + off, o);
+            }
+        } else {
+            for (uint64_t i = c_lo + threadIdx.x; i < c_hi; i += kThreads) {
+                const float w = A::read(__ldg(static_cast<const raw_t*>(P.weight) + i), 0.0f);
+                const raw_t o = A::post(__fmul_rn(__fmul_rn(hs[i - c_lo], inv), w), W);
+#pragma unroll
+                for (int j = 0; j < WCAP; ++j)
+                    if (j < W) static_cast<raw_t*>(P.out[j])[base + i] = o;
+            }
+        }
+        __syncthreads();    // the row buffer and the partials are reused by the next row
+    }
+    // Peers may still read this CTA's slice totals: leave together.
+    if (C > 1) cluster.sync();
+}
+
+template <int DT, int ALGO, int WCAP, int VB>
+static cudaError_t launch_one(const NormParams& P, dim3 grid, size_t smem, cudaStream_t s) {
+    auto k = allreduce_rmsnorm_kernel<DT, ALGO, WCAP, VB>;
+    if (smem > 48 * 1024) {
+        const cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        if (e != cudaSuccess) return e;
+    }
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = dim3(kThreads, 1, 1);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = (unsigned)P.csize;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, k, P);
+}
+
+template <int DT, int ALGO>
+static cudaError_t launch_algo(const NormParams& P, dim3 grid, size_t smem, cudaStream_t s) {
+    if (P.W <= 8) return launch_one<DT, ALGO, 8, 16>(P, grid, smem, s);
+    if (P.W <= 16) return launch_one<DT, ALGO, 16, 16>(P, grid, smem, s);
+    return launch_one<DT, ALGO, 64, 4>(P, grid, smem, s);
+}
+
+cudaError_t launch_allreduce_rmsnorm(const NormParams& P, int dtype, int algo, dim3 grid, size_t smem,
+                                     cudaStream_t s) {
+    if (dtype == MR_FP32)
+        return algo == MR_RING ? launch_algo<MR_FP32, MR_RING>(P, grid, smem, s)
+                               : launch_algo<MR_FP32, MR_TREE>(P, grid, smem, s);
+    if (dtype == MR_BF16)
+        return algo == MR_RING ? launch_algo<MR_BF16, MR_RING>(P, grid, smem, s)
+                               : launch_algo<MR_BF16, MR_TREE>(P, grid, smem, s);
+    return cudaErrorInvalidValue;
+}
+
+}  // namespace mr

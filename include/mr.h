@@ -71,7 +71,8 @@ typedef enum {
     MR_OK = 0,
     MR_ERR_INVALID_ARGUMENT = 1, /* W out of [1, 64], NULL or misaligned pointer,
                                     N % W != 0 where required, bad enum value */
-    MR_ERR_UNSUPPORTED = 2,      /* reserved: a valid request this build cannot run */
+    MR_ERR_UNSUPPORTED = 2,      /* a well-formed request outside what the call
+                                    supports (int32 for the fused RMSNorm) */
     MR_ERR_ALIAS = 3,            /* buffers overlap other than in an allowed form */
     MR_ERR_CUDA = 4              /* the CUDA runtime refused the launch */
 } mr_status_t;
@@ -105,6 +106,34 @@ mr_status_t mr_reduce_scatter(const void* const* send, void* const* recv, int W,
  */
 mr_status_t mr_all_gather(const void* const* send, void* const* recv, int W, size_t N,
                           mr_dtype_t dtype, void* stream);
+
+/*
+ * All-reduce with the residual add and RMSNorm fused after the sum [NORM]:
+ * the buffer is `rows` rows of `hidden` elements (N = rows * hidden).  For
+ * every element,
+ *     s = sum over ranks of send[r][e]   (exactly as mr_allreduce with MR_SUM
+ *                                          and `algo`: same chunks, same order,
+ *                                          fp32 accumulation)
+ *     h = s + residual[e]                  (one fp32 add; skipped if residual
+ *                                          is NULL)
+ * residual_out[e] (if non-NULL) receives h rounded to `dtype`.  For every row,
+ *     ss  = sum of h*h over the row (fp32: a per-thread partial in element
+ *           order, then a fixed tree -- the same on every run),
+ *     inv = 1 / sqrt(ss / hidden + eps),
+ *     recv[j][e] = (h * inv) * weight[e mod hidden], rounded once to dtype,
+ * for every rank j.  Each step is one IEEE fp32 operation; no FMA.
+ *   send[r], recv[r]: N elements; residual, residual_out: N elements or NULL;
+ *   weight: hidden elements (not NULL).  dtype MR_FP32 or MR_BF16 (MR_INT32
+ *   returns MR_ERR_UNSUPPORTED).  1 <= hidden <= 49152.  rows == 0 is a no-op.
+ *   In place: recv[r] == send[r], and residual_out == residual, are allowed.
+ *   The simulated ranks share one residual stream and one weight vector.
+ * [NORM] post on NCCL all-reduce, "How this survives ten thousand GPUs": in
+ * decoding, the merge (residual add) and the RMSNorm that follow the
+ * all-reduce are fused into it.
+ */
+mr_status_t mr_allreduce_rmsnorm(const void* const* send, void* const* recv, int W, size_t rows, size_t hidden,
+                                 const void* residual, void* residual_out, const void* weight, float eps,
+                                 mr_dtype_t dtype, mr_algo_t algo, void* stream);
 
 /* A static, human-readable name of a status code. */
 const char* mr_status_string(mr_status_t status);

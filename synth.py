@@ -22,6 +22,8 @@ import numpy as np
 
 TAG_GRAD = 0
 TAG_PARAM = 1
+TAG_RESIDUAL = 2
+TAG_WEIGHT = 3
 
 
 def _rng(seed: int, tag: int, r: int) -> np.random.Generator:
@@ -88,6 +90,16 @@ WORKLOADS = {
                          param_dist=("normal", 0.02)),
     # W=16 integer counts: 2^22 int32 per rank, uniform in [-1000, 1000].
     "int_counts_w16": dict(W=16, N=1 << 22, dtype="int32", dist=("uniform_int", -1000, 1000)),
+    # W=8 tensor-parallel decode step: 64 tokens x hidden 8192 bf16 partial
+    # outputs Normal(0, 1e-2) per rank, a bf16 residual stream Normal(0, 1) and
+    # an RMSNorm weight 1 + Normal(0, 0.1).
+    "tp_decode_rmsnorm_bf16_w8": dict(W=8, rows=64, hidden=8192, N=64 * 8192, dtype="bf16",
+                                      dist=("normal", 1e-2), residual_dist=("normal", 1.0),
+                                      weight_dist=("normal_mean", 1.0, 0.1)),
+    # The same at prefill size: 4096 tokens x 8192.
+    "tp_prefill_rmsnorm_bf16_w8": dict(W=8, rows=4096, hidden=8192, N=4096 * 8192, dtype="bf16",
+                                       dist=("normal", 1e-2), residual_dist=("normal", 1.0),
+                                       weight_dist=("normal_mean", 1.0, 0.1)),
     # W=8 size sweep: fp32 Normal(0, 1), N = 2^10, 2^12, ..., 2^26.
     "sweep_fp32_w8": dict(W=8, Ns=[1 << p for p in range(10, 27, 2)], dtype="fp32", dist=("normal", 1.0)),
 }
@@ -99,6 +111,13 @@ def draw(dist, seed: int, W: int, N: int, dtype: str, tag: int = TAG_GRAD):
         return uniform_int(seed, W, N, dist[1], dist[2], dtype, tag)
     if kind == "normal":
         return normal(seed, W, N, dist[1], dtype, tag)
+    if kind == "normal_mean":
+        out = []
+        for r in range(W):
+            z = _rng(seed, tag, r).standard_normal(N, dtype=np.float32)
+            z = z * np.float32(dist[2]) + np.float32(dist[1])
+            out.append(z if dtype == "fp32" else _to_bf16_bits(z))
+        return out
     raise ValueError(kind)
 
 
@@ -115,3 +134,14 @@ def workload_param_shards(name: str, seed: int = 0, N: int | None = None):
     w = WORKLOADS[name]
     n = N if N is not None else w["N"]
     return draw(w["param_dist"], seed, w["W"], n // w["W"], w["dtype"], TAG_PARAM)
+
+
+def workload_norm_operands(name: str, seed: int = 0, rows: int | None = None):
+    """(inputs, residual, weight) of a fused all-reduce + RMSNorm workload."""
+    w = WORKLOADS[name]
+    r = rows if rows is not None else w["rows"]
+    n = r * w["hidden"]
+    ins = draw(w["dist"], seed, w["W"], n, w["dtype"], TAG_GRAD)
+    res = draw(w["residual_dist"], seed, 1, n, w["dtype"], TAG_RESIDUAL)[0]
+    wt = draw(w["weight_dist"], seed, 1, w["hidden"], w["dtype"], TAG_WEIGHT)[0]
+    return ins, res, wt
