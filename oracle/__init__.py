@@ -17,6 +17,9 @@ What each routine follows (page title and section):
   * ``tree``: "The double binary tree".
   * ``chunk_lo``: Eq. (2), "Local shard bounds" (NCCL M2N).
   * ``bf16_rne``: the single bf16 rounding of an fp32 accumulator.
+  * ``sign_ef_scales`` / ``sign_ef_collective``: "Communication Optimization:
+    Gradient Compression, NCCL ..." -- 1-bit SGD (sign times ||g||_1 / d) with
+    the error feedback of its top-K section.
   * ``allreduce_rmsnorm``: "How this survives ten thousand GPUs" (post on NCCL
     all-reduce): in decoding, the merge (residual add) and the RMSNorm that
     follow the all-reduce are fused into it.
@@ -202,3 +205,42 @@ def allreduce_rmsnorm(dtype: str, algo: str, inputs, rows: int, hidden: int, wei
     if rc != 0:
         raise ValueError("oracle allreduce_rmsnorm rejected its arguments")
     return out, res_out
+
+
+def sign_ef_scales(grads, errs):
+    """s_r = ||g_r + e_r||_1 / N for every rank (fp32 values, fp64 sum)."""
+    W, N = len(grads), grads[0].size
+    _check_inputs("fp32", grads, N)
+    _check_inputs("fp32", errs, N)
+    L = lib()
+    vp, sz, i = ctypes.c_void_p, ctypes.c_size_t, ctypes.c_int
+    L.or_sign_ef_scales.argtypes = [i, sz, vp, vp, vp]
+    L.or_sign_ef_scales.restype = i
+    out = np.empty(W, np.float32)
+    if L.or_sign_ef_scales(W, N, _ptrs(grads), _ptrs(errs), out.ctypes.data) != 0:
+        raise ValueError("oracle sign_ef_scales rejected its arguments")
+    return out
+
+
+def sign_ef_collective(mode: str, op: str, algo: str, grads, errs, scales):
+    """Decode sign(g + e) * s_r, reduce (sum / avg), update the errors.
+    mode 'allreduce' or 'reduce_scatter'.  Returns (outputs, new errors); the
+    inputs are not modified."""
+    W, N = len(grads), grads[0].size
+    _check_inputs("fp32", grads, N)
+    errs = [np.array(e, dtype=np.float32, copy=True) for e in errs]
+    L = lib()
+    vp, sz, i = ctypes.c_void_p, ctypes.c_size_t, ctypes.c_int
+    L.or_sign_ef_collective.argtypes = [i, i, i, i, sz, vp, vp, vp, vp]
+    L.or_sign_ef_collective.restype = i
+    sc = np.ascontiguousarray(scales, dtype=np.float32)
+    if mode == "allreduce":
+        out = np.empty(N, np.float32)
+        outs, m = [out] * W, 0
+    else:
+        outs, m = [np.empty(N // W, np.float32) for _ in range(W)], 1
+    rc = L.or_sign_ef_collective(m, OPS[op], ALGOS[algo], W, N, _ptrs(grads), _ptrs(errs), sc.ctypes.data,
+                                 _ptrs(outs))
+    if rc != 0:
+        raise ValueError("oracle sign_ef_collective rejected its arguments")
+    return (outs[0] if m == 0 else outs), errs

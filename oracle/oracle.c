@@ -395,3 +395,59 @@ int or_allreduce_rmsnorm(int dtype, int algo, int W, size_t rows, size_t hidden,
     free(h);
     return 0;
 }
+
+/* ------------------------------------------------------------------------- */
+/* 1-bit sign compression with error feedback, then the reduction            */
+/* (Communication Optimization: Gradient Compression, NCCL ... -- the 1-bit  */
+/* SGD paragraph and the error-feedback paragraph of the top-K section)      */
+/* ------------------------------------------------------------------------- */
+
+/* p_r = g_r + e_r (one fp32 add per element), and the rank's scale
+ *     s_r = ||p_r||_1 / N,
+ * the L1 norm summed in fp64 over the whole buffer, divided in fp64 and
+ * rounded once to fp32. */
+int or_sign_ef_scales(int W, size_t N, const float* const* grad, const float* const* err, float* scales) {
+    if (W < 1 || W > OR_MAX_RANKS || N == 0) return -1;
+    for (int r = 0; r < W; r++) {
+        double l1 = 0.0;
+        for (size_t e = 0; e < N; e++) {
+            float p = grad[r][e] + err[r][e];
+            l1 += fabs((double)p);
+        }
+        scales[r] = (float)(l1 / (double)N);
+    }
+    return 0;
+}
+
+/* Given the scales: every rank's element decodes to q = +s_r if p >= 0 and
+ * -s_r otherwise (sign(p) times the scale), the carried error becomes
+ * e_r = p - q (fp32), and the decoded values are reduced exactly as the
+ * all-reduce reduces its contributions (same chunks, same ring or tree order;
+ * avg pre-scales each q by fl32(1/W)).  mode 0 writes the result to every
+ * out[j] (N elements), mode 1 writes chunk k to out[k] (N/W elements). */
+int or_sign_ef_collective(int mode, int op, int algo, int W, size_t N, const float* const* grad,
+                          float* const* err, const float* scales, void* const* out) {
+    plan_t P;
+    if (op != OR_SUM && op != OR_AVG) return -1;
+    if (make_plan(&P, OR_FP32, op, algo, W, N) != 0) return -1;
+    if (mode == 1 && N % (size_t)W != 0) return -1;
+    for (int k = 0; k < W; k++) {
+        size_t lo = or_chunk_lo(W, N, k), hi = or_chunk_lo(W, N, k + 1);
+        for (size_t e = lo; e < hi; e++) {
+            acc_t y[OR_MAX_RANKS];
+            for (int r = 0; r < W; r++) {
+                float p = grad[r][e] + err[r][e];
+                float q = (p >= 0.0f) ? scales[r] : -scales[r];
+                err[r][e] = p - q;
+                y[r].f = (op == OR_AVG) ? q * P.s : q;
+            }
+            acc_t acc = reduce_position(&P, k, e, y);
+            if (mode == 0) {
+                for (int j = 0; j < W; j++) store_result(OR_FP32, op, W, acc, out[j], e);
+            } else {
+                store_result(OR_FP32, op, W, acc, out[k], e - lo);
+            }
+        }
+    }
+    return 0;
+}

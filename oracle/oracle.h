@@ -91,6 +91,16 @@ int or_allreduce_rmsnorm(int dtype, int algo, int W, size_t rows, size_t hidden,
                          const void* const* in, const void* residual, const void* weight, double eps,
                          void* const* out, void* residual_out);
 
+/* 1-bit sign compression with error feedback (fp32 only).
+ * or_sign_ef_scales: s_r = ||g_r + e_r||_1 / N for every rank (fp64 sum).
+ * or_sign_ef_collective: with the given scales, decode q = sign(p) * s_r,
+ * update err[r] = p - q in place, and reduce the q (sum or avg) into out:
+ * mode 0 all-reduce (out[j]: N elements), mode 1 reduce-scatter (out[k]:
+ * N/W elements). */
+int or_sign_ef_scales(int W, size_t N, const float* const* grad, const float* const* err, float* scales);
+int or_sign_ef_collective(int mode, int op, int algo, int W, size_t N, const float* const* grad,
+                          float* const* err, const float* scales, void* const* out);
+
 #ifdef __cplusplus
 }
 #endif
