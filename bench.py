@@ -51,7 +51,8 @@ def parse_args():
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--e2e-steps", type=int, default=20)
     p.add_argument("--workload", default=WORKLOAD, help="a workload of synth.WORKLOADS (default: the headline)")
-    p.add_argument("--collective", choices=["allreduce", "reduce_scatter", "all_gather", "allreduce_rmsnorm"],
+    p.add_argument("--collective", choices=["allreduce", "reduce_scatter", "all_gather", "allreduce_rmsnorm",
+                                            "reduce_scatter_sign_ef", "allreduce_sign_ef"],
                    default=None,
                    help="the collective timed as one step (default: the workload's own)")
     p.add_argument("--op", default=None)
@@ -357,11 +358,13 @@ class Step:
     DEFAULTS = {"small_int_fp32_w2": ("allreduce", "sum"), "ddp_bucket_fp32_w8": ("allreduce", "avg"),
                 "fsdp_bf16_w8": ("reduce_scatter", "avg"), "int_counts_w16": ("allreduce", "sum"),
                 "sweep_fp32_w8": ("allreduce", "sum"), "tp_decode_rmsnorm_bf16_w8": ("allreduce_rmsnorm", "sum"),
-                "tp_prefill_rmsnorm_bf16_w8": ("allreduce_rmsnorm", "sum")}
+                "tp_prefill_rmsnorm_bf16_w8": ("allreduce_rmsnorm", "sum"),
+                "sign_ef_fp32_w8": ("reduce_scatter_sign_ef", "avg")}
 
     def __init__(self, args, mr, torch, dev):
         import numpy as np
         import synth
+        self.launches_per_step = 1
         self.workload = args.workload
         w = synth.WORKLOADS[self.workload]
         self.collective, op = self.DEFAULTS[self.workload]
@@ -392,6 +395,26 @@ class Step:
             self.out_bytes = sum(y.numel() * b for y in self.ys)
             self.e2e_in = self.xs + [self.res, self.wt]
             return
+        if self.collective.endswith("sign_ef"):
+            g, e = synth.workload_sign_operands(self.workload, N=N)
+            self.host_in = g + e
+            self.xs = [dev_t(h) for h in g]
+            self.err = [dev_t(h) for h in e]
+            rs = self.collective.startswith("reduce_scatter")
+            self.ys = [torch.empty(C if rs else N, dtype=tdt, device=dev) for _ in range(W)]
+            self.scales = torch.empty(W, dtype=torch.float32, device=dev)
+            self.ws = torch.empty(mr.mr_sign_ef_workspace_bytes(W, N), dtype=torch.uint8, device=dev)
+            fn = mr.mr_reduce_scatter_sign_ef if rs else mr.mr_allreduce_sign_ef
+            # two passes: read g, e for the norm; read them again, write e and the output
+            self.bytes = 5 * W * N * b + (N if rs else W * N) * b
+            self.call = lambda: fn(self.xs, self.err, self.ys, scales=self.scales, workspace=self.ws, op=self.op,
+                                   algo=self.algo)
+            self.in_bytes = 2 * W * N * b
+            self.out_bytes = sum(y.numel() * b for y in self.ys) + W * N * b
+            self.e2e_in = self.xs + self.err
+            self.e2e_extra_out = self.err
+            self.launches_per_step = 2
+            return
         if self.collective == "all_gather":
             self.host_in = synth.workload_param_shards(self.workload, N=N) if "param_dist" in w else \
                 [h[:C].copy() for h in synth.workload_inputs(self.workload, N=N)]
@@ -417,7 +440,9 @@ class Step:
     def config(self):
         kernel = {"allreduce": "fused all-reduce", "reduce_scatter": "reduce-scatter",
                   "all_gather": "all-gather",
-                  "allreduce_rmsnorm": "fused all-reduce + residual + RMSNorm"}[self.collective]
+                  "allreduce_rmsnorm": "fused all-reduce + residual + RMSNorm",
+                  "reduce_scatter_sign_ef": "1-bit sign + error feedback, then reduce-scatter (two kernels)",
+                  "allreduce_sign_ef": "1-bit sign + error feedback, then all-reduce (two kernels)"}[self.collective]
         l2 = ("inputs larger than L2, no flush" if self.in_bytes + self.out_bytes > 4 * L2_BYTES
               else "working set within 4x L2: warm-cache figure")
         return {"workload": self.workload, "collective": self.collective, "kernel": kernel, "W": self.W,
@@ -506,7 +531,7 @@ def run_mine(args):
     if dist:
         dist.barrier()
     # a graph replay launches its captured kernels without calling the library
-    launches = (mr.mr_launch_count() - launches0) if not use_graph else K
+    launches = (mr.mr_launch_count() - launches0) if not use_graph else K * S.launches_per_step
     clocks = sampler.stop()
     total_ms = t_start.elapsed_time(t_end)
     kern_ms = statistics.mean(a.elapsed_time(b) for a, b in per) / per_replay
@@ -528,13 +553,14 @@ def run_mine(args):
     if rank == 0 or world > 1:
         import numpy as np
         hin = [torch.from_numpy(np.ascontiguousarray(h).view(np.uint8)).pin_memory() for h in host]
-        hout = [torch.empty(y.numel() * y.element_size(), dtype=torch.uint8).pin_memory() for y in ys]
+        outs_e2e = list(ys) + list(getattr(S, "e2e_extra_out", []))
+        hout = [torch.empty(y.numel() * y.element_size(), dtype=torch.uint8).pin_memory() for y in outs_e2e]
 
         def e2e_step():
             for x, h in zip(S.e2e_in, hin):
                 x.view(torch.uint8).copy_(h, non_blocking=True)
             step()
-            for h, y in zip(hout, ys):
+            for h, y in zip(hout, outs_e2e):
                 h.copy_(y.view(torch.uint8), non_blocking=True)
         e2e_step()
         torch.cuda.synchronize()

@@ -17,8 +17,8 @@ import ctypes
 import os
 
 __all__ = [
-    "mr_allreduce", "mr_reduce_scatter", "mr_all_gather", "mr_allreduce_rmsnorm", "mr_status_string",
-    "mr_last_error",
+    "mr_allreduce", "mr_reduce_scatter", "mr_all_gather", "mr_allreduce_rmsnorm", "mr_allreduce_sign_ef",
+    "mr_reduce_scatter_sign_ef", "mr_sign_ef_workspace_bytes", "mr_status_string", "mr_last_error",
     "mr_allreduce_ptrs", "mr_plan_ring_order", "mr_plan_tree", "mr_chunk_lo", "mr_launch_count", "MRError",
     "load", "LIB_PATH",
     "DTYPES", "OPS", "ALGOS", "MAX_RANKS",
@@ -60,6 +60,11 @@ def load():
     L.mr_all_gather.restype = i
     L.mr_allreduce_rmsnorm.argtypes = [vp, vp, i, sz, sz, vp, vp, vp, ctypes.c_float, i, i, vp]
     L.mr_allreduce_rmsnorm.restype = i
+    L.mr_sign_ef_workspace_bytes.argtypes = [i, sz]
+    L.mr_sign_ef_workspace_bytes.restype = sz
+    for f in (L.mr_allreduce_sign_ef, L.mr_reduce_scatter_sign_ef):
+        f.argtypes = [vp, vp, vp, vp, i, sz, i, i, vp, sz, vp]
+        f.restype = i
     L.mr_status_string.argtypes = [i]
     L.mr_status_string.restype = ctypes.c_char_p
     L.mr_last_error.argtypes = []
@@ -180,6 +185,41 @@ def mr_allreduce_rmsnorm(send, recv, weight, residual=None, residual_out=None, e
                                 _code(ALGOS, algo, "algo"), _stream(stream))
     if st:
         _raise(st)
+
+
+def mr_sign_ef_workspace_bytes(W: int, N: int) -> int:
+    return int(load().mr_sign_ef_workspace_bytes(W, N))
+
+
+def _sign_ef(fn, grad, err, recv, scales, workspace, op, algo, stream):
+    import torch
+    _check(grad, "grad")
+    _check(err, "err")
+    _check(recv, "recv")
+    for t in grad + err + recv:
+        if t.dtype != torch.float32:
+            raise TypeError("sign compression takes fp32 buffers")
+    W, N = len(grad), grad[0].numel()
+    need = mr_sign_ef_workspace_bytes(W, N)
+    if workspace is None:        # plumbing: torch provides the device memory
+        workspace = torch.empty(need, dtype=torch.uint8, device=grad[0].device)
+    st = fn(_pointers(grad), _pointers(err), _pointers(recv), None if scales is None else scales.data_ptr(), W, N,
+            _code(OPS, op, "op"), _code(ALGOS, algo, "algo"), workspace.data_ptr(),
+            workspace.numel() * workspace.element_size(), _stream(stream))
+    if st:
+        _raise(st)
+
+
+def mr_allreduce_sign_ef(grad, err, recv, scales=None, workspace=None, op="avg", algo="ring", stream=None):
+    """1-bit sign compression with error feedback, then all-reduce: every
+    recv[j] gets the reduction of sign(grad[r] + err[r]) * s_r; err[r] is
+    updated in place; scales (W fp32, optional) receives s_r."""
+    _sign_ef(load().mr_allreduce_sign_ef, grad, err, recv, scales, workspace, op, algo, stream)
+
+
+def mr_reduce_scatter_sign_ef(grad, err, recv, scales=None, workspace=None, op="avg", algo="ring", stream=None):
+    """As mr_allreduce_sign_ef, but recv[k] (N/W elements) gets chunk k."""
+    _sign_ef(load().mr_reduce_scatter_sign_ef, grad, err, recv, scales, workspace, op, algo, stream)
 
 
 def mr_allreduce_ptrs(send_ptrs, recv_ptrs, N, dtype, op, algo, stream):

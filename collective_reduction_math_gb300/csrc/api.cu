@@ -97,9 +97,9 @@ mr_status_t check_op_algo(mr_op_t op, mr_algo_t algo) {
 // `allowed(a, b)` says so (an in-place form); every other pair of non-empty
 // ranges must be disjoint.  Sort by start, then sweep with the set of ranges
 // still open (which stays tiny when the buffers are disjoint).
-enum RangeKind { SEND = 0, RECV = 1, RESIDUAL = 2, RESIDUAL_OUT = 3, WEIGHT = 4 };
+enum RangeKind { SEND = 0, RECV = 1, RESIDUAL = 2, RESIDUAL_OUT = 3, WEIGHT = 4, ERR = 5, SCALES = 6, WORKSPACE = 7 };
 const char* kind_name(int k) {
-    static const char* n[] = {"send", "recv", "residual", "residual_out", "weight"};
+    static const char* n[] = {"send", "recv", "residual", "residual_out", "weight", "err", "scales", "workspace"};
     return n[k];
 }
 
@@ -112,7 +112,7 @@ struct Range {
 template <class Allowed>
 mr_status_t check_overlaps(Range* rs, int n, Allowed allowed) {
     std::sort(rs, rs + n, [](const Range& a, const Range& b) { return a.lo < b.lo; });
-    int open[2 * MR_MAX_RANKS + 8];
+    int open[3 * MR_MAX_RANKS + 8];
     int nopen = 0;
     for (int i = 0; i < n; ++i) {
         int keep = 0;
@@ -383,6 +383,114 @@ mr_status_t mr_allreduce_rmsnorm(const void* const* send, void* const* recv, int
         fprintf(stderr, "[mr] allreduce_rmsnorm dtype=%s algo=%s W=%d rows=%zu hidden=%zu vector=%d grid=%u "
                 "cluster=%d smem=%zu\n", dtype_name(dtype), algo_name(algo), W, rows, hidden, P.vec, grid.x, csize, smem);
     return MR_OK;
+}
+
+size_t mr_sign_ef_workspace_bytes(int W, size_t N) {
+    if (W < 1 || W > MR_MAX_RANKS) return 0;
+    return (size_t)W * (size_t)mr::sign_blocks(N) * sizeof(double);
+}
+
+static mr_status_t run_sign_ef(const char* what, int mode, const void* const* grad, void* const* err,
+                               void* const* recv, float* scales, int W, size_t N, mr_op_t op, mr_algo_t algo,
+                               void* workspace, size_t workspace_bytes, void* stream) {
+    g_last_error.clear();
+    mr_status_t st = check_common(grad, recv, W, MR_FP32);
+    if (st == MR_OK) st = check_op_algo(op, algo);
+    if (st != MR_OK) return st;
+    if (op != MR_SUM && op != MR_AVG) return fail(MR_ERR_UNSUPPORTED, "%s reduces with sum or avg only", what);
+    if (!err) return fail(MR_ERR_INVALID_ARGUMENT, "err pointer array is NULL");
+    if (mode == mr::MODE_REDUCE_SCATTER && N % (size_t)W != 0)
+        return fail(MR_ERR_INVALID_ARGUMENT, "%s needs N (%zu) divisible by W (%d)", what, N, W);
+    if (N == 0) return MR_OK;
+    if ((st = check_pointers(grad, recv, W, MR_FP32)) != MR_OK) return st;
+    for (int r = 0; r < W; ++r)
+        if (!err[r] || ((uintptr_t)err[r] & 3u)) return fail(MR_ERR_INVALID_ARGUMENT, "err[%d] is NULL or misaligned", r);
+    if ((uintptr_t)scales & 3u) return fail(MR_ERR_INVALID_ARGUMENT, "scales is misaligned");
+    const size_t need = mr_sign_ef_workspace_bytes(W, N);
+    if (!workspace || ((uintptr_t)workspace & 7u) || workspace_bytes < need)
+        return fail(MR_ERR_INVALID_ARGUMENT, "workspace must be 8-byte aligned and hold %zu bytes", need);
+
+    const size_t bytes = N * 4, C = N / (size_t)W, out_bytes = mode == mr::MODE_REDUCE_SCATTER ? C * 4 : bytes;
+    Range rs[3 * MR_MAX_RANKS + 2];
+    int n = 0;
+    for (int r = 0; r < W; ++r) {
+        rs[n++] = {(uintptr_t)grad[r], (uintptr_t)grad[r] + bytes, r, SEND};
+        rs[n++] = {(uintptr_t)recv[r], (uintptr_t)recv[r] + out_bytes, r, RECV};
+        rs[n++] = {(uintptr_t)err[r], (uintptr_t)err[r] + bytes, r, ERR};
+    }
+    if (scales) rs[n++] = {(uintptr_t)scales, (uintptr_t)scales + (size_t)W * 4, 0, SCALES};
+    rs[n++] = {(uintptr_t)workspace, (uintptr_t)workspace + need, 0, WORKSPACE};
+    st = check_overlaps(rs, n, [&](const Range& x, const Range& y) {
+        if (!(x.kind == SEND && y.kind == RECV && x.rank == y.rank)) return false;
+        if (mode == mr::MODE_REDUCE_SCATTER) return y.lo == x.lo + (size_t)x.rank * C * 4;
+        return y.lo == x.lo;
+    });
+    if (st != MR_OK) return st;
+
+    mr::SignParams P;
+    for (int r = 0; r < W; ++r) {
+        P.grad[r] = grad[r];
+        P.err[r] = err[r];
+        P.out[r] = recv[r];
+    }
+    P.partials = static_cast<double*>(workspace);
+    P.scales = scales;
+    P.N = N;
+    P.W = W;
+    P.mode = mode;
+    P.nb = mr::sign_blocks(N);
+    P.avg = (float)(1.0 / (double)W);
+    P.nseg = plan_segments(W, N, algo, P.seg);
+    const int vb = mr::sign_vector_bytes(W);
+    bool vec = true, l1_vec = true;
+    for (int r = 0; r < W; ++r) {
+        vec = vec && ((uintptr_t)grad[r] % vb == 0) && ((uintptr_t)err[r] % vb == 0) && ((uintptr_t)recv[r] % vb == 0);
+        l1_vec = l1_vec && ((uintptr_t)grad[r] % 16 == 0) && ((uintptr_t)err[r] % 16 == 0);
+    }
+    if (mode == mr::MODE_REDUCE_SCATTER) vec = vec && (C * 4) % vb == 0;
+    P.vec = vec ? 1 : 0;
+    P.l1_vec = l1_vec ? 1 : 0;
+    // tiles of kThreads vectors (or elements), round-robin across segments
+    const uint64_t lanes = vb / 4;
+    P.tile_start[0] = 0;
+    P.tiles_max = 0;
+    for (int i = 0; i < P.nseg; ++i) {
+        const mr::Segment& g = P.seg[i];
+        uint64_t units = g.hi - g.lo;
+        if (P.vec) {
+            const uint64_t va = (g.lo + lanes - 1) / lanes, vb2 = g.hi / lanes;
+            units = va < vb2 ? vb2 - va : 0;
+        }
+        P.tile_start[i + 1] = P.tile_start[i] + (units + mr::kThreads - 1) / mr::kThreads;
+        P.tiles_max = std::max(P.tiles_max, P.tile_start[i + 1] - P.tile_start[i]);
+    }
+    const uint64_t tiles = std::max<uint64_t>(P.vec ? P.tiles_max * P.nseg : P.tile_start[P.nseg], P.nseg);
+    const dim3 grid((unsigned)std::min<uint64_t>((uint64_t)sm_count() * 2, tiles), 1, 1);
+    cudaError_t e = mr::launch_sign_l1(P, (cudaStream_t)stream);
+    if (e == cudaSuccess) {
+        g_launches.fetch_add(1, std::memory_order_relaxed);
+        e = mr::launch_sign_ef(P, op, algo, grid, (cudaStream_t)stream);
+        if (e == cudaSuccess) g_launches.fetch_add(1, std::memory_order_relaxed);
+    }
+    if (e != cudaSuccess) return fail(MR_ERR_CUDA, "%s launch failed: %s", what, cudaGetErrorString(e));
+    if (debug_level() > 0)
+        fprintf(stderr, "[mr] %s op=%s algo=%s W=%d N=%zu l1_blocks=%d vector=%d grid=%u\n", what, op_name(op),
+                algo_name(algo), W, N, P.nb, P.vec, grid.x);
+    return MR_OK;
+}
+
+mr_status_t mr_allreduce_sign_ef(const void* const* grad, void* const* err, void* const* recv, float* scales,
+                                 int W, size_t N, mr_op_t op, mr_algo_t algo, void* workspace,
+                                 size_t workspace_bytes, void* stream) {
+    return run_sign_ef("allreduce_sign_ef", mr::MODE_ALLREDUCE, grad, err, recv, scales, W, N, op, algo, workspace,
+                       workspace_bytes, stream);
+}
+
+mr_status_t mr_reduce_scatter_sign_ef(const void* const* grad, void* const* err, void* const* recv, float* scales,
+                                      int W, size_t N, mr_op_t op, mr_algo_t algo, void* workspace,
+                                      size_t workspace_bytes, void* stream) {
+    return run_sign_ef("reduce_scatter_sign_ef", mr::MODE_REDUCE_SCATTER, grad, err, recv, scales, W, N, op, algo,
+                       workspace, workspace_bytes, stream);
 }
 
 const char* mr_status_string(mr_status_t status) {

@@ -59,6 +59,36 @@ struct NormParams {
 // Largest row the fused RMSNorm keeps in shared memory (fp32 per element).
 constexpr uint64_t kMaxNormHidden = 49152;
 
+// 1-bit sign compression with error feedback (fp32).
+struct SignParams {
+    const void* grad[kMaxRanks];
+    void* err[kMaxRanks];       // read, then overwritten with the new residual
+    void* out[kMaxRanks];
+    double* partials;           // workspace: W x nb per-block L1 partials
+    float* scales;              // W scales out (device)
+    Segment seg[kMaxSegments];
+    uint64_t tile_start[kMaxSegments + 1];
+    uint64_t tiles_max;
+    uint64_t N;
+    int W;
+    int nseg;
+    int mode;
+    int vec;                    // 1: every pointer (and reduce-scatter chunk start) aligned to
+                                //    sign_vector_bytes(W): the decode kernel's vector path
+    int l1_vec;                 // 1: grad and err 16-byte aligned: the L1 kernel's 16-byte loads
+    int nb;                     // L1 blocks per rank
+    float avg;                  // fl32(1/W)
+};
+
+// L1 blocks per rank for a buffer of N elements (the workspace holds W*nb doubles).
+constexpr uint64_t kSignMaxBlocks = 256;
+inline int sign_blocks(uint64_t N) {
+    const uint64_t nb = (N + 8191) / 8192;
+    return (int)(nb < 1 ? 1 : nb > kSignMaxBlocks ? kSignMaxBlocks : nb);
+}
+// Vector width of the decode-and-reduce kernel for a given W.
+constexpr int sign_vector_bytes(int W) { return W <= 8 ? 16 : W <= 16 ? 8 : 4; }
+
 struct GatherParams {
     const void* in[kMaxRanks];
     void* out[kMaxRanks];
@@ -86,6 +116,8 @@ cudaError_t launch_reduce_fp32(const ReduceParams& P, int op, int algo, dim3 gri
 cudaError_t launch_reduce_bf16(const ReduceParams& P, int op, int algo, dim3 grid, cudaStream_t s);
 cudaError_t launch_reduce_int32(const ReduceParams& P, int op, int algo, dim3 grid, cudaStream_t s);
 cudaError_t launch_all_gather(const GatherParams& P, dim3 grid, cudaStream_t s);
+cudaError_t launch_sign_l1(const SignParams& P, cudaStream_t s);
+cudaError_t launch_sign_ef(const SignParams& P, int op, int algo, dim3 grid, cudaStream_t s);
 cudaError_t launch_allreduce_rmsnorm(const NormParams& P, int dtype, int algo, dim3 grid, size_t smem, cudaStream_t s);
 
 }  // namespace mr

@@ -135,6 +135,47 @@ mr_status_t mr_allreduce_rmsnorm(const void* const* send, void* const* recv, int
                                  const void* residual, void* residual_out, const void* weight, float eps,
                                  mr_dtype_t dtype, mr_algo_t algo, void* stream);
 
+/*
+ * 1-bit sign compression with error feedback, then the reduction [SIGN]
+ * (fp32 only).  For every rank r and element e:
+ *     p = grad[r][e] + err[r][e]                 (one fp32 add)
+ *     s_r = ||p_r||_1 / N                        (L1 norm of the whole rank
+ *                                                 buffer: per-thread compensated
+ *                                                 fp32 sums, an fp64 tree per
+ *                                                 block, the block partials
+ *                                                 added in order in fp64, one
+ *                                                 fp64 divide, one rounding to
+ *                                                 fp32 -- the same on every run)
+ *     q = +s_r if p >= 0 else -s_r               (the 1-bit code, decoded)
+ *     err[r][e] = p - q                          (what was not sent: carried to
+ *                                                 the next step)
+ * and the q are reduced across ranks exactly as mr_allreduce reduces its
+ * contributions (op MR_SUM or MR_AVG -- avg pre-scales each q by fl32(1/W) --,
+ * same chunks, same ring or tree order):
+ *   mr_allreduce_sign_ef:      recv[j] (N elements) gets the result, every j;
+ *                              in place: recv[r] == grad[r].
+ *   mr_reduce_scatter_sign_ef: recv[k] (N/W elements) gets chunk k; N % W == 0;
+ *                              in place: recv[r] == grad[r] + r*N/W.
+ *   grad[r]: N elements (read); err[r]: N elements (read, then overwritten);
+ *   scales: W floats of device memory, receives s_r (may be NULL);
+ *   workspace: device memory of at least mr_sign_ef_workspace_bytes(W, N)
+ *   bytes, owned by the caller, 8-byte aligned; its contents need no
+ *   initialisation and are scratch after the call.  Calls that share a
+ *   workspace must not run concurrently.  Other ops return
+ *   MR_ERR_UNSUPPORTED.  Two kernels are launched on `stream`.
+ * [SIGN] "Communication Optimization: Gradient Compression, NCCL ..."
+ * (mbrenndoerfer.com): 1-bit SGD sends sign(g) with the scale ||g||_1 / d;
+ * error feedback compresses g plus the residual owed from the previous step
+ * and keeps the part that was not sent.
+ */
+size_t mr_sign_ef_workspace_bytes(int W, size_t N);
+mr_status_t mr_allreduce_sign_ef(const void* const* grad, void* const* err, void* const* recv, float* scales,
+                                 int W, size_t N, mr_op_t op, mr_algo_t algo, void* workspace,
+                                 size_t workspace_bytes, void* stream);
+mr_status_t mr_reduce_scatter_sign_ef(const void* const* grad, void* const* err, void* const* recv, float* scales,
+                                      int W, size_t N, mr_op_t op, mr_algo_t algo, void* workspace,
+                                      size_t workspace_bytes, void* stream);
+
 /* A static, human-readable name of a status code. */
 const char* mr_status_string(mr_status_t status);
 

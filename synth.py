@@ -24,6 +24,7 @@ TAG_GRAD = 0
 TAG_PARAM = 1
 TAG_RESIDUAL = 2
 TAG_WEIGHT = 3
+TAG_ERR = 4
 
 
 def _rng(seed: int, tag: int, r: int) -> np.random.Generator:
@@ -100,6 +101,9 @@ WORKLOADS = {
     "tp_prefill_rmsnorm_bf16_w8": dict(W=8, rows=4096, hidden=8192, N=4096 * 8192, dtype="bf16",
                                        dist=("normal", 1e-2), residual_dist=("normal", 1.0),
                                        weight_dist=("normal_mean", 1.0, 0.1)),
+    # W=8 DDP bucket sent as 1-bit signs with error feedback: 2^24 fp32
+    # gradients Normal(0, 1e-3) and a carried residual Normal(0, 1e-4).
+    "sign_ef_fp32_w8": dict(W=8, N=1 << 24, dtype="fp32", dist=("normal", 1e-3), err_dist=("normal", 1e-4)),
     # W=8 size sweep: fp32 Normal(0, 1), N = 2^10, 2^12, ..., 2^26.
     "sweep_fp32_w8": dict(W=8, Ns=[1 << p for p in range(10, 27, 2)], dtype="fp32", dist=("normal", 1.0)),
 }
@@ -145,3 +149,11 @@ def workload_norm_operands(name: str, seed: int = 0, rows: int | None = None):
     res = draw(w["residual_dist"], seed, 1, n, w["dtype"], TAG_RESIDUAL)[0]
     wt = draw(w["weight_dist"], seed, 1, w["hidden"], w["dtype"], TAG_WEIGHT)[0]
     return ins, res, wt
+
+
+def workload_sign_operands(name: str, seed: int = 0, N: int | None = None):
+    """(gradients, residuals) of a sign-compression workload."""
+    w = WORKLOADS[name]
+    n = N if N is not None else w["N"]
+    return (draw(w["dist"], seed, w["W"], n, w["dtype"], TAG_GRAD),
+            draw(w["err_dist"], seed, w["W"], n, w["dtype"], TAG_ERR))
