@@ -18,7 +18,8 @@ import os
 
 __all__ = [
     "mr_allreduce", "mr_reduce_scatter", "mr_all_gather", "mr_allreduce_rmsnorm", "mr_allreduce_sign_ef",
-    "mr_reduce_scatter_sign_ef", "mr_sign_ef_workspace_bytes", "mr_status_string", "mr_last_error",
+    "mr_reduce_scatter_sign_ef", "mr_reduce_scatter_sign_ef_noalloc", "mr_sign_ef_workspace_bytes",
+    "mr_status_string", "mr_last_error",
     "mr_allreduce_ptrs", "mr_plan_ring_order", "mr_plan_tree", "mr_chunk_lo", "mr_launch_count", "MRError",
     "load", "LIB_PATH",
     "DTYPES", "OPS", "ALGOS", "MAX_RANKS",
@@ -65,6 +66,8 @@ def load():
     for f in (L.mr_allreduce_sign_ef, L.mr_reduce_scatter_sign_ef):
         f.argtypes = [vp, vp, vp, vp, i, sz, i, i, vp, sz, vp]
         f.restype = i
+    L.mr_reduce_scatter_sign_ef_noalloc.argtypes = [vp, vp, vp, vp, i, sz, i, i, vp]
+    L.mr_reduce_scatter_sign_ef_noalloc.restype = i
     L.mr_status_string.argtypes = [i]
     L.mr_status_string.restype = ctypes.c_char_p
     L.mr_last_error.argtypes = []
@@ -220,6 +223,20 @@ def mr_allreduce_sign_ef(grad, err, recv, scales=None, workspace=None, op="avg",
 def mr_reduce_scatter_sign_ef(grad, err, recv, scales=None, workspace=None, op="avg", algo="ring", stream=None):
     """As mr_allreduce_sign_ef, but recv[k] (N/W elements) gets chunk k."""
     _sign_ef(load().mr_reduce_scatter_sign_ef, grad, err, recv, scales, workspace, op, algo, stream)
+
+
+def mr_reduce_scatter_sign_ef_noalloc(grad, err, recv, scales=None, op="avg", algo="ring", stream=None):
+    """mr_reduce_scatter_sign_ef without a workspace argument: the library
+    uses its own fixed 64 KiB scratch, for callers that cannot allocate device
+    memory.  Concurrent calls race on that scratch."""
+    _check(grad, "grad")
+    _check(err, "err")
+    _check(recv, "recv")
+    st = load().mr_reduce_scatter_sign_ef_noalloc(
+        _pointers(grad), _pointers(err), _pointers(recv), None if scales is None else scales.data_ptr(), len(grad),
+        grad[0].numel(), _code(OPS, op, "op"), _code(ALGOS, algo, "algo"), _stream(stream))
+    if st:
+        _raise(st)
 
 
 def mr_allreduce_ptrs(send_ptrs, recv_ptrs, N, dtype, op, algo, stream):

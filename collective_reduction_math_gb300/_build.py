@@ -20,7 +20,7 @@ BUILD = os.path.join(ROOT, "_build", "mr")
 LIB = os.path.join(HERE, "libmr.so")
 
 SOURCES = ["api.cu", "reduce_fp32.cu", "reduce_bf16.cu", "reduce_int32.cu", "all_gather.cu", "rmsnorm_kernel.cu",
-           "sign_ef_kernel.cu"]
+           "sign_ef_kernel.cu", "sign_ef_noalloc.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ARCH + ["-O3", "-lineinfo", "-std=c++17", "-fmad=false", "-Xcompiler", "-fPIC,-O2",
                 "-I", INCLUDE, "-I", CSRC]

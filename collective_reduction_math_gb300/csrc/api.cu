@@ -232,6 +232,20 @@ mr_status_t run_reduce(const char* what, int mode, const void* const* send, void
 
 }  // namespace
 
+namespace mr {
+// Records `fmt` as the calling thread's last error and returns `st` (for
+// entry points defined in other translation units).
+mr_status_t report_error(mr_status_t st, const char* fmt, ...) {
+    char buf[512];
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(buf, sizeof(buf), fmt, ap);
+    va_end(ap);
+    g_last_error = buf;
+    return st;
+}
+}  // namespace mr
+
 extern "C" {
 
 mr_status_t mr_allreduce(const void* const* send, void* const* recv, int W, size_t N, mr_dtype_t dtype,

@@ -116,6 +116,7 @@ cudaError_t launch_reduce_fp32(const ReduceParams& P, int op, int algo, dim3 gri
 cudaError_t launch_reduce_bf16(const ReduceParams& P, int op, int algo, dim3 grid, cudaStream_t s);
 cudaError_t launch_reduce_int32(const ReduceParams& P, int op, int algo, dim3 grid, cudaStream_t s);
 cudaError_t launch_all_gather(const GatherParams& P, dim3 grid, cudaStream_t s);
+mr_status_t report_error(mr_status_t st, const char* fmt, ...);
 cudaError_t launch_sign_l1(const SignParams& P, cudaStream_t s);
 cudaError_t launch_sign_ef(const SignParams& P, int op, int algo, dim3 grid, cudaStream_t s);
 cudaError_t launch_allreduce_rmsnorm(const NormParams& P, int dtype, int algo, dim3 grid, size_t smem, cudaStream_t s);

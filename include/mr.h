@@ -176,6 +176,30 @@ mr_status_t mr_reduce_scatter_sign_ef(const void* const* grad, void* const* err,
                                       int W, size_t N, mr_op_t op, mr_algo_t algo, void* workspace,
                                       size_t workspace_bytes, void* stream);
 
+/*
+ * mr_reduce_scatter_sign_ef_noalloc: mr_reduce_scatter_sign_ef for callers
+ * that cannot allocate device memory -- for example a plugin that is handed
+ * only the tensors it works on, a runtime whose device memory belongs to
+ * another allocator, or a latency-critical loop that cannot pay for
+ * cudaMalloc's implicit synchronisation.  The pages have no counterpart: this
+ * is an interface variant, not part of the method.
+ *   Same arguments, results and errors as mr_reduce_scatter_sign_ef, without
+ *   the workspace: the scratch is a 64 KiB array of device memory inside the
+ *   library (every GPU that loads the library holds it until the process
+ *   exits).  W * (blocks of N) partials must fit in it: every N for W <= 32,
+ *   and up to 2^20 elements per rank at W = 64; larger requests return
+ *   MR_ERR_INVALID_ARGUMENT and name the limit in mr_last_error().  Nothing
+ *   here calls cudaMalloc, cudaFree or any allocating routine.
+ *   The first call on each device looks up the array's device address (with
+ *   that device current); make that first call before any stream capture.
+ *   Every call uses the same array: each call writes all the partials it
+ *   later reads, so nothing needs clearing between calls, but calls that
+ *   overlap on the GPU (other streams, other threads) race on it.
+ */
+mr_status_t mr_reduce_scatter_sign_ef_noalloc(const void* const* grad, void* const* err, void* const* recv,
+                                              float* scales, int W, size_t N, mr_op_t op, mr_algo_t algo,
+                                              void* stream);
+
 /* A static, human-readable name of a status code. */
 const char* mr_status_string(mr_status_t status);
 
