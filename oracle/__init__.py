@@ -40,7 +40,7 @@ _LIB_PATH = os.path.join(_HERE, "liboracle.so")
 
 DTYPES = {"fp32": 0, "bf16": 1, "int32": 2}
 OPS = {"sum": 0, "prod": 1, "min": 2, "max": 3, "avg": 4}
-ALGOS = {"ring": 0, "tree": 1}
+ALGOS = {"ring": 0, "tree": 1, "hier": 2}
 NP_DTYPE = {"fp32": np.float32, "bf16": np.uint16, "int32": np.int32}
 
 _lib = None
@@ -244,3 +244,38 @@ def sign_ef_collective(mode: str, op: str, algo: str, grads, errs, scales):
     if rc != 0:
         raise ValueError("oracle sign_ef_collective rejected its arguments")
     return (outs[0] if m == 0 else outs), errs
+
+
+def allreduce_ex(dtype: str, op: str, algo: str, inputs, group: int = 0, hop: bool = False,
+                 all_ranks: bool = False):
+    """All-reduce with a choice of order: algo 'hier' needs ``group`` (ranks
+    per group, dividing W); ``hop`` rounds a bf16 running total to bf16 after
+    every combine."""
+    W, N = len(inputs), inputs[0].size
+    _check_inputs(dtype, inputs, N)
+    L = lib()
+    vp, sz, i = ctypes.c_void_p, ctypes.c_size_t, ctypes.c_int
+    L.or_allreduce_ex.argtypes = [i, i, i, i, i, i, sz, vp, vp]
+    L.or_allreduce_ex.restype = i
+    copies = W if all_ranks else 1
+    outs = [np.empty(N, NP_DTYPE[dtype]) for _ in range(copies)]
+    rc = L.or_allreduce_ex(DTYPES[dtype], OPS[op], ALGOS[algo], group, int(hop), W, N, _ptrs(inputs),
+                           _ptrs([outs[j % copies] for j in range(W)]))
+    if rc != 0:
+        raise ValueError("oracle allreduce_ex rejected its arguments")
+    return outs if all_ranks else outs[0]
+
+
+def reduce_scatter_ex(dtype: str, op: str, algo: str, inputs, group: int = 0, hop: bool = False):
+    W, N = len(inputs), inputs[0].size
+    _check_inputs(dtype, inputs, N)
+    L = lib()
+    vp, sz, i = ctypes.c_void_p, ctypes.c_size_t, ctypes.c_int
+    L.or_reduce_scatter_ex.argtypes = [i, i, i, i, i, i, sz, vp, vp]
+    L.or_reduce_scatter_ex.restype = i
+    outs = [np.empty(N // W, NP_DTYPE[dtype]) for _ in range(W)]
+    rc = L.or_reduce_scatter_ex(DTYPES[dtype], OPS[op], ALGOS[algo], group, int(hop), W, N, _ptrs(inputs),
+                                _ptrs(outs))
+    if rc != 0:
+        raise ValueError("oracle reduce_scatter_ex rejected its arguments")
+    return outs

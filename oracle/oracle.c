@@ -219,16 +219,7 @@ int or_tree_build(int W, int which, int* parent, int* child) {
     return tree2_rank(W, 0);
 }
 
-/* Reduce up the tree, each parent adding its children's subtotals to its own
- * contribution: subtotal(v) = y_v (+) subtotal(first child) (+) subtotal(second). */
-static acc_t tree_subtotal(int dtype, int op, int v, const int* child, const acc_t* y) {
-    acc_t acc = y[v];
-    for (int i = 0; i < 2; i++) {
-        int c = child[2 * v + i];
-        if (c >= 0) acc = combine(dtype, op, acc, tree_subtotal(dtype, op, c, child, y));
-    }
-    return acc;
-}
+
 
 /* ------------------------------------------------------------------------- */
 /* The reduction of one element position                                     */
@@ -236,21 +227,46 @@ static acc_t tree_subtotal(int dtype, int op, int v, const int* child, const acc
 
 typedef struct {
     int dtype, op, algo, W;
+    int group;   /* ranks per group (hierarchical order) */
+    int hop;     /* 1: round the running total to bf16 after every hop (bf16 only) */
     size_t N;
     float s;
     int root[2];
     int child[2][2 * OR_MAX_RANKS];
 } plan_t;
 
-static int make_plan(plan_t* P, int dtype, int op, int algo, int W, size_t N) {
+/* Per-hop rounding: with hop set, a bf16 running total is rounded to bf16
+ * after every combine, as when each partial crosses a wire as bf16. */
+static acc_t hop_round(const plan_t* P, acc_t a) {
+    if (P->hop && P->dtype == OR_BF16) a.u = (uint32_t)or_f32_to_bf16_rne(a.f) << 16;
+    return a;
+}
+
+static acc_t combine_hop(const plan_t* P, acc_t a, acc_t b) { return hop_round(P, combine(P->dtype, P->op, a, b)); }
+
+/* Reduce up the tree, each parent adding its children's subtotals to its own
+ * contribution: subtotal(v) = y_v (+) subtotal(first child) (+) subtotal(second). */
+static acc_t tree_subtotal(const plan_t* P, int v, const int* child, const acc_t* y) {
+    acc_t acc = y[v];
+    for (int i = 0; i < 2; i++) {
+        int c = child[2 * v + i];
+        if (c >= 0) acc = combine_hop(P, acc, tree_subtotal(P, c, child, y));
+    }
+    return acc;
+}
+
+static int make_plan_ex(plan_t* P, int dtype, int op, int algo, int group, int hop, int W, size_t N) {
     int parent[OR_MAX_RANKS];
     if (W < 1 || W > OR_MAX_RANKS) return -1;
     if (dtype < OR_FP32 || dtype > OR_INT32) return -1;
     if (op < OR_SUM || op > OR_AVG) return -1;
-    if (algo != OR_RING && algo != OR_TREE) return -1;
+    if (algo != OR_RING && algo != OR_TREE && algo != OR_HIER) return -1;
+    if (algo == OR_HIER && (group < 1 || W % group != 0)) return -1;
     P->dtype = dtype;
     P->op = op;
     P->algo = algo;
+    P->group = algo == OR_HIER ? group : W;
+    P->hop = hop ? 1 : 0;
     P->W = W;
     P->N = N;
     P->s = avg_scale(W);
@@ -259,23 +275,52 @@ static int make_plan(plan_t* P, int dtype, int op, int algo, int W, size_t N) {
     return 0;
 }
 
+static int make_plan(plan_t* P, int dtype, int op, int algo, int W, size_t N) {
+    return make_plan_ex(P, dtype, op, algo, W, 0, W, N);
+}
+
 /* y[r] = rank r's (pre-scaled) contribution at element e, which lies in chunk k. */
 static acc_t reduce_position(const plan_t* P, int k, size_t e, const acc_t* y) {
     if (P->algo == OR_RING) {
         int order[OR_MAX_RANKS];
         or_ring_order(P->W, k, order);
         acc_t acc = y[order[0]];
-        for (int i = 1; i < P->W; i++) acc = combine(P->dtype, P->op, acc, y[order[i]]);
+        for (int i = 1; i < P->W; i++) acc = combine_hop(P, acc, y[order[i]]);
         return acc;
+    }
+    if (P->algo == OR_HIER) {
+        /* Hierarchical all-reduce ("Communication Optimization ...", the
+         * five-step topology-aware all-reduce): ranks form G = W/g groups of g
+         * (rank a*g + i is local rank i of group a).  A ring reduce-scatter
+         * inside each group leaves chunk c (of g) summed over the group on
+         * local rank c -- its ring order is i = c+1, ..., c; a ring all-reduce
+         * across the groups then cuts chunk c into G pieces and sums piece d
+         * over the groups in order a = d+1, ..., d; the all-gather inside the
+         * groups copies. */
+        int g = P->group, G = P->W / g, c = 0, d = 0;
+        int og[OR_MAX_RANKS], oG[OR_MAX_RANKS];
+        while (or_chunk_lo(g, P->N, c + 1) <= e) c++;
+        size_t clo = or_chunk_lo(g, P->N, c), clen = or_chunk_lo(g, P->N, c + 1) - clo;
+        while (clo + or_chunk_lo(G, clen, d + 1) <= e) d++;
+        or_ring_order(g, c, og);
+        or_ring_order(G, d, oG);
+        acc_t total;
+        for (int ia = 0; ia < G; ia++) {
+            int a = oG[ia];
+            acc_t part = y[a * g + og[0]];
+            for (int ii = 1; ii < g; ii++) part = combine_hop(P, part, y[a * g + og[ii]]);
+            total = ia ? combine_hop(P, total, part) : part;
+        }
+        return total;
     }
     /* The first floor(N/2) elements climb tree 1, the rest tree 2. */
     int t = (e < P->N / 2) ? 0 : 1;
-    return tree_subtotal(P->dtype, P->op, P->root[t], P->child[t], y);
+    return tree_subtotal(P, P->root[t], P->child[t], y);
 }
 
 static acc_t reduce_from_buffers(const plan_t* P, int k, size_t e, const void* const* in) {
     acc_t y[OR_MAX_RANKS];
-    for (int r = 0; r < P->W; r++) y[r] = read_contribution(P->dtype, P->op, P->s, in[r], e);
+    for (int r = 0; r < P->W; r++) y[r] = hop_round(P, read_contribution(P->dtype, P->op, P->s, in[r], e));
     return reduce_position(P, k, e, y);
 }
 
@@ -283,10 +328,10 @@ static acc_t reduce_from_buffers(const plan_t* P, int k, size_t e, const void* c
 /* The collectives                                                           */
 /* ------------------------------------------------------------------------- */
 
-int or_allreduce(int dtype, int op, int algo, int W, size_t N,
-                 const void* const* in, void* const* out) {
+int or_allreduce_ex(int dtype, int op, int algo, int group, int hop, int W, size_t N,
+                    const void* const* in, void* const* out) {
     plan_t P;
-    if (make_plan(&P, dtype, op, algo, W, N) != 0) return -1;
+    if (make_plan_ex(&P, dtype, op, algo, group, hop, W, N) != 0) return -1;
     for (int k = 0; k < W; k++) {
         size_t lo = or_chunk_lo(W, N, k), hi = or_chunk_lo(W, N, k + 1);
         for (size_t e = lo; e < hi; e++) {
@@ -297,10 +342,10 @@ int or_allreduce(int dtype, int op, int algo, int W, size_t N,
     return 0;
 }
 
-int or_reduce_scatter(int dtype, int op, int algo, int W, size_t N,
-                      const void* const* in, void* const* out) {
+int or_reduce_scatter_ex(int dtype, int op, int algo, int group, int hop, int W, size_t N,
+                         const void* const* in, void* const* out) {
     plan_t P;
-    if (make_plan(&P, dtype, op, algo, W, N) != 0) return -1;
+    if (make_plan_ex(&P, dtype, op, algo, group, hop, W, N) != 0) return -1;
     if (N % (size_t)W != 0) return -1;
     for (int k = 0; k < W; k++) {
         size_t lo = or_chunk_lo(W, N, k), hi = or_chunk_lo(W, N, k + 1);
@@ -310,6 +355,16 @@ int or_reduce_scatter(int dtype, int op, int algo, int W, size_t N,
         }
     }
     return 0;
+}
+
+int or_allreduce(int dtype, int op, int algo, int W, size_t N, const void* const* in, void* const* out) {
+    if (algo == OR_HIER) return -1;
+    return or_allreduce_ex(dtype, op, algo, W, 0, W, N, in, out);
+}
+
+int or_reduce_scatter(int dtype, int op, int algo, int W, size_t N, const void* const* in, void* const* out) {
+    if (algo == OR_HIER) return -1;
+    return or_reduce_scatter_ex(dtype, op, algo, W, 0, W, N, in, out);
 }
 
 int or_all_gather(int dtype, int W, size_t N, const void* const* in, void* const* out) {

@@ -42,7 +42,7 @@ extern "C" {
 
 enum { OR_FP32 = 0, OR_BF16 = 1, OR_INT32 = 2 };
 enum { OR_SUM = 0, OR_PROD = 1, OR_MIN = 2, OR_MAX = 3, OR_AVG = 4 };
-enum { OR_RING = 0, OR_TREE = 1 };
+enum { OR_RING = 0, OR_TREE = 1, OR_HIER = 2 };
 
 #define OR_MAX_RANKS 64
 
@@ -76,6 +76,15 @@ int or_reduce_scatter(int dtype, int op, int algo, int W, size_t N,
                       const void* const* in, void* const* out);
 int or_all_gather(int dtype, int W, size_t N,
                   const void* const* in, void* const* out);
+
+/* The same with a choice of order: algo OR_RING, OR_TREE or OR_HIER (groups
+ * of `group` ranks, W % group == 0: ring reduce-scatter inside the groups,
+ * ring all-reduce across them); hop = 1 rounds a bf16 running total to bf16
+ * after every combine (no effect for fp32 and int32). */
+int or_allreduce_ex(int dtype, int op, int algo, int group, int hop, int W, size_t N,
+                    const void* const* in, void* const* out);
+int or_reduce_scatter_ex(int dtype, int op, int algo, int group, int hop, int W, size_t N,
+                         const void* const* in, void* const* out);
 
 /* Reduce a single element position: y[0..W-1] are rank r's raw values at
  * global element e of an N-element buffer (used to check sampled outputs of

@@ -12,7 +12,7 @@ import numpy as np
 
 
 def _widen(dtype, a):
-    if dtype == "bf16":
+    if dtype == "bf16" and a.dtype == np.uint16:     # raw bf16 bits; fp32 values pass through
         return (a.astype(np.uint32) << 16).view(np.float32)
     return a.copy()
 
@@ -28,15 +28,28 @@ def _post(dtype, op, W, acc):
     return acc
 
 
-def _combine(dtype, op, received, own):
+def _to_bf16_and_back(x):
+    import torch
+    t = torch.from_numpy(np.ascontiguousarray(x, dtype=np.float32)).to(torch.bfloat16).float()
+    return t.numpy()
+
+
+def _combine(dtype, op, received, own, hop=False):
     if op in ("sum", "avg"):
-        return received + own          # numpy: fp32 rounded add / int32 wrap
-    if op == "prod":
-        return received * own
-    raise ValueError("the simulator covers the order-dependent ops only")
+        r = received + own             # numpy: fp32 rounded add / int32 wrap
+    elif op == "prod":
+        r = received * own
+    else:
+        raise ValueError("the simulator covers the order-dependent ops only")
+    if hop and dtype == "bf16":        # the partial crosses the wire as bf16
+        r = _to_bf16_and_back(r)
+    return r
 
 
-def simulate(dtype, op, inputs):
+def simulate(dtype, op, inputs, hop=False, raw=False):
+    """hop: round a bf16 running total to bf16 after every add (and the
+    pre-scaled contributions of avg).  raw: skip the postOp and return fp32
+    running totals (used to chain simulations)."""
     """Returns (per-rank result buffers, number of link transfers, and for
     each chunk the rank on which its total completed)."""
     W, N = len(inputs), inputs[0].size
@@ -45,12 +58,15 @@ def simulate(dtype, op, inputs):
         if op == "avg" and dtype != "int32":
             s = np.float32(1.0 / W)
             y = [v * s for v in y]
+            if hop and dtype == "bf16":
+                y = [_to_bf16_and_back(v) for v in y]
         bounds = [(k * N) // W for k in range(W + 1)]
         chunk = [slice(bounds[k], bounds[k + 1]) for k in range(W)]
-        out_dtype = inputs[0].dtype
+        post = (lambda a: a) if raw else (lambda a: _post(dtype, op, W, a))
+        out_dtype = y[0].dtype if raw else inputs[0].dtype
         result = [np.empty(N, out_dtype) for _ in range(W)]
         if W == 1:
-            result[0][:] = _post(dtype, op, W, y[0])
+            result[0][:] = post(y[0])
             return result, 0, [0]
 
         transfers = 0
@@ -70,13 +86,13 @@ def simulate(dtype, op, inputs):
             outgoing = []
             for r in range(W):
                 c, data = inbox[r]
-                outgoing.append((c, _combine(dtype, op, data, y[r][chunk[c]])))
+                outgoing.append((c, _combine(dtype, op, data, y[r][chunk[c]], hop)))
             deliver(outgoing)
         # the arriving chunk completes here: postOp, keep, forward
         outgoing = []
         for r in range(W):
             c, data = inbox[r]
-            fin = _post(dtype, op, W, _combine(dtype, op, data, y[r][chunk[c]]))
+            fin = post(_combine(dtype, op, data, y[r][chunk[c]], hop))
             result[r][chunk[c]] = fin
             finisher[c] = r
             outgoing.append((c, fin))
