@@ -37,7 +37,7 @@ FALLBACK_HBM_GBS = 6800.0
 L2_BYTES = 129 * 1000 * 1000
 GRAPH_BELOW_BYTES = 256 << 20     # steps moving less than this are timed as CUDA-graph replays
 GRAPH_STEPS = 50
-KERNEL_SOURCES = ["reduce_kernel.cuh", "order.cuh", "mr_internal.h", "reduce_fp32.cu", "api.cu"]
+KERNEL_SOURCES = ["reduce_kernel.cuh", "order.cuh", "mr_internal.h", "reduce_fp32_ring.cu", "api.cu"]
 PROFILE = os.path.join(ROOT, "profiles", "reduce_kernel_ddp_bucket_fp32_w8.txt")
 
 
@@ -56,7 +56,9 @@ def parse_args():
                    default=None,
                    help="the collective timed as one step (default: the workload's own)")
     p.add_argument("--op", default=None)
-    p.add_argument("--algo", default="ring")
+    p.add_argument("--algo", default="ring", choices=["ring", "tree", "hier"])
+    p.add_argument("--group", type=int, default=None, help="ranks per group for --algo hier")
+    p.add_argument("--per-hop", action="store_true", help="round a bf16 running total to bf16 after every hop")
     p.add_argument("--n", type=int, default=None, help="elements per rank (sweep workload)")
     return p.parse_args()
 
@@ -359,7 +361,7 @@ class Step:
                 "fsdp_bf16_w8": ("reduce_scatter", "avg"), "int_counts_w16": ("allreduce", "sum"),
                 "sweep_fp32_w8": ("allreduce", "sum"), "tp_decode_rmsnorm_bf16_w8": ("allreduce_rmsnorm", "sum"),
                 "tp_prefill_rmsnorm_bf16_w8": ("allreduce_rmsnorm", "sum"),
-                "sign_ef_fp32_w8": ("reduce_scatter_sign_ef", "avg")}
+                "sign_ef_fp32_w8": ("reduce_scatter_sign_ef", "avg"), "hier_bf16_w16": ("allreduce", "avg")}
 
     def __init__(self, args, mr, torch, dev):
         import numpy as np
@@ -371,6 +373,9 @@ class Step:
         self.collective = args.collective or self.collective
         self.op = args.op or op
         self.algo = args.algo
+        self.group = args.group
+        self.per_hop = args.per_hop
+        ex = self.algo == "hier" or self.per_hop
         self.W = W = w["W"]
         self.N = N = args.n or w.get("N") or w["Ns"][-1]
         self.dtype = w["dtype"]
@@ -428,11 +433,19 @@ class Step:
             if self.collective == "allreduce":
                 self.ys = [torch.empty_like(x) for x in self.xs]
                 self.bytes = 2 * W * N * b
-                self.call = lambda: mr.mr_allreduce(self.xs, self.ys, op=self.op, algo=self.algo)
+                if ex:
+                    self.call = lambda: mr.mr_allreduce_ex(self.xs, self.ys, op=self.op, algo=self.algo,
+                                                           group=self.group, per_hop=self.per_hop)
+                else:
+                    self.call = lambda: mr.mr_allreduce(self.xs, self.ys, op=self.op, algo=self.algo)
             else:
                 self.ys = [torch.empty(C, dtype=tdt, device=dev) for _ in range(W)]
                 self.bytes = (W + 1) * N * b
-                self.call = lambda: mr.mr_reduce_scatter(self.xs, self.ys, op=self.op, algo=self.algo)
+                if ex:
+                    self.call = lambda: mr.mr_reduce_scatter_ex(self.xs, self.ys, op=self.op, algo=self.algo,
+                                                                group=self.group, per_hop=self.per_hop)
+                else:
+                    self.call = lambda: mr.mr_reduce_scatter(self.xs, self.ys, op=self.op, algo=self.algo)
         self.in_bytes = sum(x.numel() * b for x in self.xs)
         self.out_bytes = sum(y.numel() * b for y in self.ys)
         self.e2e_in = self.xs
@@ -447,7 +460,9 @@ class Step:
               else "working set within 4x L2: warm-cache figure")
         return {"workload": self.workload, "collective": self.collective, "kernel": kernel, "W": self.W,
                 "N_per_rank": self.N, "dtype": self.dtype, "op": self.op if self.collective != "all_gather" else None,
-                "algo": self.algo if self.collective != "all_gather" else None, "bytes_per_step": self.bytes,
+                "algo": self.algo if self.collective != "all_gather" else None,
+                "group": self.group if self.algo == "hier" else None, "per_hop_rounding": self.per_hop,
+                "bytes_per_step": self.bytes,
                 "l2": l2}
 
 

@@ -17,7 +17,7 @@ import ctypes
 import os
 
 __all__ = [
-    "mr_allreduce", "mr_reduce_scatter", "mr_all_gather", "mr_allreduce_rmsnorm", "mr_allreduce_sign_ef",
+    "mr_allreduce", "mr_reduce_scatter", "mr_all_gather", "mr_allreduce_ex", "mr_reduce_scatter_ex", "mr_allreduce_rmsnorm", "mr_allreduce_sign_ef",
     "mr_reduce_scatter_sign_ef", "mr_reduce_scatter_sign_ef_noalloc", "mr_sign_ef_workspace_bytes",
     "mr_status_string", "mr_last_error",
     "mr_allreduce_ptrs", "mr_plan_ring_order", "mr_plan_tree", "mr_chunk_lo", "mr_launch_count", "MRError",
@@ -29,10 +29,15 @@ LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libmr.so")
 MAX_RANKS = 64
 DTYPES = {"fp32": 0, "bf16": 1, "int32": 2}
 OPS = {"sum": 0, "prod": 1, "min": 2, "max": 3, "avg": 4}
-ALGOS = {"ring": 0, "tree": 1}
+ALGOS = {"ring": 0, "tree": 1, "hier": 2}
 STATUS = {0: "MR_OK", 1: "MR_ERR_INVALID_ARGUMENT", 2: "MR_ERR_UNSUPPORTED", 3: "MR_ERR_ALIAS", 4: "MR_ERR_CUDA"}
 
 _lib = None
+
+
+class Order(ctypes.Structure):
+    """mr_order_t: accumulation order for mr_allreduce_ex / mr_reduce_scatter_ex."""
+    _fields_ = [("algo", ctypes.c_int), ("group", ctypes.c_int), ("per_hop_rounding", ctypes.c_int)]
 
 
 class MRError(RuntimeError):
@@ -68,6 +73,9 @@ def load():
         f.restype = i
     L.mr_reduce_scatter_sign_ef_noalloc.argtypes = [vp, vp, vp, vp, i, sz, i, i, vp]
     L.mr_reduce_scatter_sign_ef_noalloc.restype = i
+    for f in (L.mr_allreduce_ex, L.mr_reduce_scatter_ex):
+        f.argtypes = [vp, vp, i, sz, i, i, ctypes.POINTER(Order), vp]
+        f.restype = i
     L.mr_status_string.argtypes = [i]
     L.mr_status_string.restype = ctypes.c_char_p
     L.mr_last_error.argtypes = []
@@ -165,6 +173,36 @@ def mr_all_gather(send, recv, stream=None):
     L = load()
     st = L.mr_all_gather(_pointers(send), _pointers(recv), len(send), recv[0].numel(), _dtype_code(recv[0]),
                          _stream(stream))
+    if st:
+        _raise(st)
+
+
+def _order(algo, group, per_hop):
+    return Order(_code(ALGOS, algo, "algo"), int(group or 0), 1 if per_hop else 0)
+
+
+def mr_allreduce_ex(send, recv, op="sum", algo="ring", group=None, per_hop=False, stream=None):
+    """All-reduce with a choice of order: algo 'hier' folds groups of
+    ``group`` consecutive ranks first, then the group totals; ``per_hop``
+    rounds a bf16 running total to bf16 after every combine."""
+    _check(send, "send")
+    _check(recv, "recv")
+    L = load()
+    o = _order(algo, group, per_hop)
+    st = L.mr_allreduce_ex(_pointers(send), _pointers(recv), len(send), send[0].numel(), _dtype_code(send[0]),
+                           _code(OPS, op, "op"), ctypes.byref(o), _stream(stream))
+    if st:
+        _raise(st)
+
+
+def mr_reduce_scatter_ex(send, recv, op="sum", algo="ring", group=None, per_hop=False, stream=None):
+    """Reduce-scatter with a choice of order (see mr_allreduce_ex)."""
+    _check(send, "send")
+    _check(recv, "recv")
+    L = load()
+    o = _order(algo, group, per_hop)
+    st = L.mr_reduce_scatter_ex(_pointers(send), _pointers(recv), len(send), send[0].numel(), _dtype_code(send[0]),
+                                _code(OPS, op, "op"), ctypes.byref(o), _stream(stream))
     if st:
         _raise(st)
 

@@ -45,7 +45,7 @@ const char* op_name(mr_op_t op) {
     static const char* n[] = {"sum", "prod", "min", "max", "avg"};
     return n[op];
 }
-const char* algo_name(mr_algo_t a) { return a == MR_RING ? "ring" : "tree"; }
+const char* algo_name(mr_algo_t a) { return a == MR_RING ? "ring" : a == MR_TREE ? "tree" : "hier"; }
 
 // Streaming multiprocessors of the current device (cached per device).
 int sm_count() {
@@ -89,6 +89,8 @@ mr_status_t check_pointers(const void* const* send, void* const* recv, int W, mr
 
 mr_status_t check_op_algo(mr_op_t op, mr_algo_t algo) {
     if (op < MR_SUM || op > MR_AVG) return fail(MR_ERR_INVALID_ARGUMENT, "unknown op %d", (int)op);
+    if (algo == MR_HIER)
+        return fail(MR_ERR_INVALID_ARGUMENT, "MR_HIER needs a group size: use mr_allreduce_ex / mr_reduce_scatter_ex");
     if (algo != MR_RING && algo != MR_TREE) return fail(MR_ERR_INVALID_ARGUMENT, "unknown algo %d", (int)algo);
     return MR_OK;
 }
@@ -155,10 +157,10 @@ int plan_segments(int W, uint64_t N, mr_algo_t algo, mr::Segment* seg) {
         const uint64_t lo = mr::chunk_lo(W, N, k), hi = mr::chunk_lo(W, N, k + 1);
         if (lo == hi) continue;
         if (algo == MR_TREE && lo < half && half < hi) {
-            seg[n++] = {lo, half, lo, k, 0};
-            seg[n++] = {half, hi, lo, k, 1};
+            seg[n++] = {lo, half, lo, k, 0, 0, 0};
+            seg[n++] = {half, hi, lo, k, 1, 0, 0};
         } else {
-            seg[n++] = {lo, hi, lo, k, (algo == MR_TREE && lo >= half) ? 1 : 0};
+            seg[n++] = {lo, hi, lo, k, (algo == MR_TREE && lo >= half) ? 1 : 0, 0, 0};
         }
     }
     return n;
@@ -167,6 +169,35 @@ int plan_segments(int W, uint64_t N, mr_algo_t algo, mr::Segment* seg) {
 // Tile counts per segment (prefix sums into P.tile_start, the largest in
 // P.tiles_max) and the 1-D grid: a few CTAs per SM, never more than there are
 // tiles.
+// Segments of the hierarchical order: each chunk c of `group` chunks cut into
+// its G = W / group pieces; for reduce-scatter also cut at the W chunk bounds,
+// which place the output.
+int plan_segments_hier(int W, uint64_t N, int group, bool cut_at_chunks, mr::Segment* seg) {
+    const int G = W / group;
+    uint64_t b[2 * MR_MAX_RANKS + 2];
+    int nb = 0;
+    for (int c = 0; c < group; ++c) {
+        const uint64_t clo = mr::chunk_lo(group, N, c), clen = mr::chunk_lo(group, N, c + 1) - clo;
+        for (int d = 0; d < G; ++d) b[nb++] = clo + mr::chunk_lo(G, clen, d);
+    }
+    b[nb++] = N;
+    if (cut_at_chunks)
+        for (int k = 1; k < W; ++k) b[nb++] = mr::chunk_lo(W, N, k);
+    std::sort(b, b + nb);
+    nb = (int)(std::unique(b, b + nb) - b);
+    int n = 0, k = 0, c = 0, d = 0;
+    for (int i = 0; i + 1 < nb; ++i) {
+        const uint64_t lo = b[i], hi = b[i + 1];
+        if (lo == hi) continue;
+        while (mr::chunk_lo(W, N, k + 1) <= lo) ++k;
+        while (mr::chunk_lo(group, N, c + 1) <= lo) { ++c; d = 0; }
+        const uint64_t clo = mr::chunk_lo(group, N, c), clen = mr::chunk_lo(group, N, c + 1) - clo;
+        while (clo + mr::chunk_lo(G, clen, d + 1) <= lo) ++d;
+        seg[n++] = {lo, hi, mr::chunk_lo(W, N, k), k, 0, c, d};
+    }
+    return n;
+}
+
 dim3 plan_tiles(mr::ReduceParams& P, int lanes) {
     const bool rs = P.mode == mr::MODE_REDUCE_SCATTER;
     const int u = mr::reduce_unroll(P.W, rs);
@@ -193,15 +224,24 @@ dim3 plan_tiles(mr::ReduceParams& P, int lanes) {
 cudaError_t launch_reduce(mr_dtype_t dtype, const mr::ReduceParams& P, mr_op_t op, mr_algo_t algo,
                           dim3 grid, cudaStream_t s) {
     switch (dtype) {
-        case MR_FP32: return mr::launch_reduce_fp32(P, op, algo, grid, s);
-        case MR_BF16: return mr::launch_reduce_bf16(P, op, algo, grid, s);
-        case MR_INT32: return mr::launch_reduce_int32(P, op, algo, grid, s);
+        case MR_FP32:
+            return algo == MR_RING ? mr::launch_reduce_fp32_ring(P, op, grid, s)
+                 : algo == MR_TREE ? mr::launch_reduce_fp32_tree(P, op, grid, s)
+                                   : mr::launch_reduce_fp32_hier(P, op, grid, s);
+        case MR_BF16:
+            return algo == MR_RING ? mr::launch_reduce_bf16_ring(P, op, grid, s)
+                 : algo == MR_TREE ? mr::launch_reduce_bf16_tree(P, op, grid, s)
+                                   : mr::launch_reduce_bf16_hier(P, op, grid, s);
+        case MR_INT32:
+            return algo == MR_RING ? mr::launch_reduce_int32_ring(P, op, grid, s)
+                 : algo == MR_TREE ? mr::launch_reduce_int32_tree(P, op, grid, s)
+                                   : mr::launch_reduce_int32_hier(P, op, grid, s);
     }
     return cudaErrorInvalidValue;
 }
 
 mr_status_t run_reduce(const char* what, int mode, const void* const* send, void* const* recv, int W, size_t N,
-                       mr_dtype_t dtype, mr_op_t op, mr_algo_t algo, void* stream) {
+                       mr_dtype_t dtype, mr_op_t op, mr_algo_t algo, void* stream, int group = 0, int hop = 0) {
     mr::ReduceParams P;
     for (int r = 0; r < W; ++r) {
         P.in[r] = send[r];
@@ -210,7 +250,12 @@ mr_status_t run_reduce(const char* what, int mode, const void* const* send, void
     P.W = W;
     P.mode = mode;
     P.scale = (float)(1.0 / (double)W);
-    P.nseg = plan_segments(W, N, algo, P.seg);
+    P.group = algo == MR_HIER ? group : W;
+    P.hop = hop;
+    P.gmask = 0;
+    for (int p = 0; p < W; p += P.group) P.gmask |= 1ull << p;
+    P.nseg = algo == MR_HIER ? plan_segments_hier(W, N, group, mode == mr::MODE_REDUCE_SCATTER, P.seg)
+                             : plan_segments(W, N, algo, P.seg);
     const int vb = mr::reduce_vector_bytes(W);
     const int eb = (int)elem_bytes(dtype);
     bool vec = true;
@@ -224,8 +269,9 @@ mr_status_t run_reduce(const char* what, int mode, const void* const* send, void
         return fail(MR_ERR_CUDA, "%s launch failed: %s", what, cudaGetErrorString(err));
     g_launches.fetch_add(1, std::memory_order_relaxed);
     if (debug_level() > 0)
-        fprintf(stderr, "[mr] %s dtype=%s op=%s algo=%s W=%d N=%zu segments=%d tiles=%llu vector=%d grid=%u threads=%d\n",
-                what, dtype_name(dtype), op_name(op), algo_name(algo), W, N, P.nseg,
+        fprintf(stderr, "[mr] %s dtype=%s op=%s algo=%s group=%d per_hop=%d W=%d N=%zu segments=%d tiles=%llu "
+                "vector=%d grid=%u threads=%d\n",
+                what, dtype_name(dtype), op_name(op), algo_name(algo), P.group, P.hop, W, N, P.nseg,
                 (unsigned long long)P.tile_start[P.nseg], P.vec, grid.x, mr::kThreads);
     return MR_OK;
 }
@@ -317,6 +363,61 @@ mr_status_t mr_all_gather(const void* const* send, void* const* recv, int W, siz
         fprintf(stderr, "[mr] all_gather dtype=%s W=%d N=%zu vector=%d grid=%u threads=%d\n", dtype_name(dtype),
                 W, N, P.vec, grid.x, mr::kThreads);
     return MR_OK;
+}
+
+static mr_status_t check_order(const mr_order_t* order, int W, mr_algo_t* algo, int* group, int* hop) {
+    *algo = MR_RING;
+    *group = W;
+    *hop = 0;
+    if (!order) return MR_OK;
+    if (order->algo != MR_RING && order->algo != MR_TREE && order->algo != MR_HIER)
+        return fail(MR_ERR_INVALID_ARGUMENT, "unknown algo %d", (int)order->algo);
+    if (order->per_hop_rounding != 0 && order->per_hop_rounding != 1)
+        return fail(MR_ERR_INVALID_ARGUMENT, "per_hop_rounding must be 0 or 1");
+    if (order->algo == MR_HIER && (order->group < 1 || order->group > W || W % order->group != 0))
+        return fail(MR_ERR_INVALID_ARGUMENT, "group = %d must divide W = %d", order->group, W);
+    *algo = order->algo;
+    *group = order->algo == MR_HIER ? order->group : W;
+    *hop = order->per_hop_rounding;
+    return MR_OK;
+}
+
+mr_status_t mr_allreduce_ex(const void* const* send, void* const* recv, int W, size_t N, mr_dtype_t dtype,
+                            mr_op_t op, const mr_order_t* order, void* stream) {
+    g_last_error.clear();
+    mr_algo_t algo;
+    int group, hop;
+    mr_status_t st = check_common(send, recv, W, dtype);
+    if (st == MR_OK) st = check_op_algo(op, MR_RING);
+    if (st == MR_OK) st = check_order(order, W, &algo, &group, &hop);
+    if (st != MR_OK || N == 0) return st;
+    if ((st = check_pointers(send, recv, W, dtype)) != MR_OK) return st;
+    const size_t bytes = N * elem_bytes(dtype);
+    st = check_alias(send, bytes, recv, bytes, W, [&](int r) { return send[r] == recv[r]; });
+    if (st != MR_OK) return st;
+    return run_reduce("allreduce_ex", mr::MODE_ALLREDUCE, send, recv, W, N, dtype, op, algo, stream, group, hop);
+}
+
+mr_status_t mr_reduce_scatter_ex(const void* const* send, void* const* recv, int W, size_t N, mr_dtype_t dtype,
+                                 mr_op_t op, const mr_order_t* order, void* stream) {
+    g_last_error.clear();
+    mr_algo_t algo;
+    int group, hop;
+    mr_status_t st = check_common(send, recv, W, dtype);
+    if (st == MR_OK) st = check_op_algo(op, MR_RING);
+    if (st == MR_OK) st = check_order(order, W, &algo, &group, &hop);
+    if (st != MR_OK) return st;
+    if (N % (size_t)W != 0)
+        return fail(MR_ERR_INVALID_ARGUMENT, "reduce_scatter needs N (%zu) divisible by W (%d)", N, W);
+    if (N == 0) return MR_OK;
+    if ((st = check_pointers(send, recv, W, dtype)) != MR_OK) return st;
+    const size_t b = elem_bytes(dtype), C = N / (size_t)W;
+    st = check_alias(send, N * b, recv, C * b, W, [&](int r) {
+        return (const char*)recv[r] == (const char*)send[r] + (size_t)r * C * b;
+    });
+    if (st != MR_OK) return st;
+    return run_reduce("reduce_scatter_ex", mr::MODE_REDUCE_SCATTER, send, recv, W, N, dtype, op, algo, stream, group,
+                      hop);
 }
 
 mr_status_t mr_allreduce_rmsnorm(const void* const* send, void* const* recv, int W, size_t rows, size_t hidden,

@@ -10,7 +10,7 @@
 namespace mr {
 
 constexpr int kMaxRanks = MR_MAX_RANKS;
-constexpr int kMaxSegments = MR_MAX_RANKS + 1;
+constexpr int kMaxSegments = 2 * MR_MAX_RANKS + 2;
 constexpr int kThreads = 256;       // threads per CTA for every kernel
 constexpr int kGatherUnroll = 8;        // 16-byte vectors per thread per all-gather tile
 constexpr int kGatherBlocksPerSm = 16;  // all-gather CTAs per SM in the grid (several waves)
@@ -22,6 +22,7 @@ struct Segment {
     uint64_t out_lo;    // reduce-scatter: element e goes to recv[k][e - out_lo]
     int32_t k;          // the chunk (its owner rank)
     int32_t tree;       // 0: tree 1, 1: tree 2 (tree algorithm only)
+    int32_t hc, hd;     // hierarchical order: chunk of `group`, piece of that chunk
 };
 
 enum { MODE_ALLREDUCE = 0, MODE_REDUCE_SCATTER = 1 };
@@ -38,6 +39,9 @@ struct ReduceParams {
     int vec;        // 1: every pointer (and every reduce-scatter chunk start) is
                     // aligned to the vector width, so the vector path may run
     float scale;    // fl32(1/W): the float avg pre-scale
+    int group;      // hierarchical order: ranks per group
+    int hop;        // 1: round a bf16 running total to bf16 after every combine
+    uint64_t gmask; // hierarchical order: bit p set where order position p starts a group
 };
 
 // All-reduce + residual + RMSNorm (rows x hidden elements).
@@ -112,9 +116,18 @@ constexpr int reduce_unroll_for(int wcap, bool rs) {
 constexpr int reduce_unroll(int W, bool rs) { return reduce_unroll_for(reduce_wcap(W), rs); }
 constexpr int reduce_blocks_per_sm(int wcap, int u) { return (wcap <= 8 && wcap * u <= 8) ? 3 : 2; }
 
-cudaError_t launch_reduce_fp32(const ReduceParams& P, int op, int algo, dim3 grid, cudaStream_t s);
-cudaError_t launch_reduce_bf16(const ReduceParams& P, int op, int algo, dim3 grid, cudaStream_t s);
-cudaError_t launch_reduce_int32(const ReduceParams& P, int op, int algo, dim3 grid, cudaStream_t s);
+#define MR_DECLARE_REDUCE(dt, algo) \
+    cudaError_t launch_reduce_##dt##_##algo(const ReduceParams& P, int op, dim3 grid, cudaStream_t s);
+MR_DECLARE_REDUCE(fp32, ring)
+MR_DECLARE_REDUCE(fp32, tree)
+MR_DECLARE_REDUCE(fp32, hier)
+MR_DECLARE_REDUCE(bf16, ring)
+MR_DECLARE_REDUCE(bf16, tree)
+MR_DECLARE_REDUCE(bf16, hier)
+MR_DECLARE_REDUCE(int32, ring)
+MR_DECLARE_REDUCE(int32, tree)
+MR_DECLARE_REDUCE(int32, hier)
+#undef MR_DECLARE_REDUCE
 cudaError_t launch_all_gather(const GatherParams& P, dim3 grid, cudaStream_t s);
 mr_status_t report_error(mr_status_t st, const char* fmt, ...);
 cudaError_t launch_sign_l1(const SignParams& P, cudaStream_t s);

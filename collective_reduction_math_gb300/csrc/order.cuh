@@ -73,6 +73,15 @@ MR_HD int tree_parent(int W, int p) {
     return q < W ? q : (p & ~b);
 }
 
+// Hierarchical order (groups of g consecutive ranks, G = W/g groups):
+// position p = (group position) * g + (local position); the group at group
+// position j is (d+1+j) mod G, the local rank at local position i is
+// (c+1+i) mod g, where c is the element's chunk of g and d its piece of G.
+MR_HD int hier_rank(int W, int g, int c, int d, int p) {
+    const int G = W / g;
+    return ring_rank(G, d, p / g) * g + ring_rank(g, c, p % g);
+}
+
 // floor(k*N/W) without forming k*N.
 MR_HD uint64_t chunk_lo(int W, uint64_t N, int k) {
     uint64_t q = N / (uint64_t)W, r = N % (uint64_t)W;

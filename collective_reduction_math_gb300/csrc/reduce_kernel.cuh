@@ -79,6 +79,13 @@ template <int DT, int OP> struct Arith {
         }
     }
 
+    // Per-hop rounding: a bf16 running total rounded to bf16 (as it would
+    // cross a wire); the identity for fp32 and int32.
+    static __device__ __forceinline__ acc_t hop(acc_t a) {
+        if constexpr (DT == MR_BF16) return __uint_as_float((uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(a)) << 16);
+        else return a;
+    }
+
     // The postOp where the sum completes.
     static __device__ __forceinline__ raw_t post(acc_t a, int W) {
         if constexpr (DT == MR_FP32) return __float_as_uint(a);
@@ -95,13 +102,20 @@ template <int DT, int OP> struct Arith {
 // first W positions are valid.  All register indices are compile-time.
 // ---------------------------------------------------------------------------
 
+// `hop`: round the running total after every combine (bf16 per-hop order).
+template <class A>
+__device__ __forceinline__ typename A::acc_t comb(typename A::acc_t a, typename A::acc_t b, bool hop) {
+    typename A::acc_t r = A::combine(a, b);
+    return hop ? A::hop(r) : r;
+}
+
 // Ring: a left fold in chunk order.
 template <class A, int WCAP>
-__device__ __forceinline__ typename A::acc_t fold_ring(const typename A::acc_t (&y)[WCAP], int W) {
+__device__ __forceinline__ typename A::acc_t fold_ring(const typename A::acc_t (&y)[WCAP], int W, bool hop) {
     typename A::acc_t a = y[0];
 #pragma unroll
     for (int i = 1; i < WCAP; ++i)
-        if (i < W) a = A::combine(a, y[i]);
+        if (i < W) a = comb<A>(a, y[i], hop);
     return a;
 }
 
@@ -109,18 +123,18 @@ __device__ __forceinline__ typename A::acc_t fold_ring(const typename A::acc_t (
 // complete before its parent uses it; each node takes its own value, then its
 // lower child's subtotal, then its upper child's; the root takes its one child.
 template <class A, int WCAP>
-__device__ __forceinline__ typename A::acc_t fold_tree(typename A::acc_t (&y)[WCAP], int W) {
+__device__ __forceinline__ typename A::acc_t fold_tree(typename A::acc_t (&y)[WCAP], int W, bool hop) {
 #pragma unroll
     for (int b = 2; b < WCAP; b <<= 1) {
 #pragma unroll
         for (int p = b; p < WCAP; p += 2 * b) {
             if (p < W) {
-                typename A::acc_t a = A::combine(y[p], y[p - b / 2]);
+                typename A::acc_t a = comb<A>(y[p], y[p - b / 2], hop);
                 bool taken = false;
 #pragma unroll
                 for (int h = b / 2; h >= 1; h >>= 1) {
                     if (!taken && p + h < W) {
-                        a = A::combine(a, y[p + h]);
+                        a = comb<A>(a, y[p + h], hop);
                         taken = true;
                     }
                 }
@@ -133,17 +147,42 @@ __device__ __forceinline__ typename A::acc_t fold_tree(typename A::acc_t (&y)[WC
 #pragma unroll
     for (int h = WCAP / 2; h >= 1; h >>= 1) {
         if (!taken && h < W) {
-            a = A::combine(a, y[h]);
+            a = comb<A>(a, y[h], hop);
             taken = true;
         }
     }
     return a;
 }
 
+// Hierarchical: positions come group by group (gmask marks the first position
+// of each group); each group's positions are folded left to right, then the
+// group totals left to right.
+template <class A, int WCAP>
+__device__ __forceinline__ typename A::acc_t fold_hier(const typename A::acc_t (&y)[WCAP], int W, uint64_t gmask,
+                                                       bool hop) {
+    typename A::acc_t part = y[0], total = y[0];
+    bool have_total = false;
+#pragma unroll
+    for (int i = 1; i < WCAP; ++i) {
+        if (i < W) {
+            if ((gmask >> i) & 1u) {
+                total = have_total ? comb<A>(total, part, hop) : part;
+                have_total = true;
+                part = y[i];
+            } else {
+                part = comb<A>(part, y[i], hop);
+            }
+        }
+    }
+    return have_total ? comb<A>(total, part, hop) : part;
+}
+
 template <class A, int ALGO, int WCAP>
-__device__ __forceinline__ typename A::acc_t fold(typename A::acc_t (&y)[WCAP], int W) {
-    if constexpr (ALGO == MR_RING) return fold_ring<A, WCAP>(y, W);
-    else return fold_tree<A, WCAP>(y, W);
+__device__ __forceinline__ typename A::acc_t fold(typename A::acc_t (&y)[WCAP], int W, bool hop = false,
+                                                  uint64_t gmask = 0) {
+    if constexpr (ALGO == MR_RING) return fold_ring<A, WCAP>(y, W, hop);
+    else if constexpr (ALGO == MR_TREE) return fold_tree<A, WCAP>(y, W, hop);
+    else return fold_hier<A, WCAP>(y, W, gmask, hop);
 }
 
 // ---------------------------------------------------------------------------
@@ -198,9 +237,10 @@ template <class raw_t, int VB> __device__ __forceinline__ void set_lane(Vec<VB>&
 
 // Rank at order position i of segment sg.
 template <int ALGO>
-__device__ __forceinline__ int order_rank(int W, const Segment& sg, int i) {
+__device__ __forceinline__ int order_rank(int W, const Segment& sg, int i, int group = 1) {
     if constexpr (ALGO == MR_RING) return ring_rank(W, sg.k, i);
-    else return tree_rank(W, sg.tree, i);
+    else if constexpr (ALGO == MR_TREE) return tree_rank(W, sg.tree, i);
+    else return hier_rank(W, group, sg.hc, sg.hd, i);
 }
 
 template <int DT, int OP, int ALGO, int WCAP, int VB, int U>
@@ -215,6 +255,13 @@ reduce_kernel(const __grid_constant__ ReduceParams P) {
     const int W = P.W;
     const float s = P.scale;
     const bool rs = (P.mode == MODE_REDUCE_SCATTER);
+    const bool hop = DT == MR_BF16 && P.hop;
+    const uint64_t gmask = P.gmask;
+    // a contribution as read: widened, pre-scaled, and for per-hop bf16 rounded
+    auto contrib = [&](raw_t x) -> acc_t {
+        const acc_t y = A::read(x, s);
+        return (OP == MR_AVG && hop) ? A::hop(y) : y;
+    };
 
     // Input pointers in the current segment's accumulation order: in
     // registers for up to 16 ranks, in a shared-memory table beyond that.
@@ -228,12 +275,12 @@ reduce_kernel(const __grid_constant__ ReduceParams P) {
         if constexpr (kTable) {
             __syncthreads();
             if (threadIdx.x < W)
-                table[threadIdx.x] = static_cast<const char*>(P.in[order_rank<ALGO>(W, P.seg[seg], threadIdx.x)]);
+                table[threadIdx.x] = static_cast<const char*>(P.in[order_rank<ALGO>(W, P.seg[seg], threadIdx.x, P.group)]);
             __syncthreads();
         } else {
 #pragma unroll
             for (int i = 0; i < WCAP; ++i)
-                src[i] = (i < W) ? static_cast<const char*>(P.in[order_rank<ALGO>(W, P.seg[seg], i)]) : nullptr;
+                src[i] = (i < W) ? static_cast<const char*>(P.in[order_rank<ALGO>(W, P.seg[seg], i, P.group)]) : nullptr;
         }
     };
     auto input = [&](int i) -> const char* {
@@ -246,8 +293,8 @@ reduce_kernel(const __grid_constant__ ReduceParams P) {
         acc_t y[WCAP];
 #pragma unroll
         for (int i = 0; i < WCAP; ++i)
-            if (i < W) y[i] = A::read(__ldg(reinterpret_cast<const raw_t*>(input(i)) + e), s);
-        const raw_t r = A::post(fold<A, ALGO, WCAP>(y, W), W);
+            if (i < W) y[i] = contrib(__ldg(reinterpret_cast<const raw_t*>(input(i)) + e));
+        const raw_t r = A::post(fold<A, ALGO, WCAP>(y, W, hop, gmask), W);
         if (rs) {
             static_cast<raw_t*>(P.out[sg.k])[e - sg.out_lo] = r;
         } else {
@@ -296,8 +343,8 @@ reduce_kernel(const __grid_constant__ ReduceParams P) {
                     acc_t y[WCAP];
 #pragma unroll
                     for (int i = 0; i < WCAP; ++i)
-                        if (i < W) y[i] = A::read(get_lane<raw_t, VB>(raw[u][i], l), s);
-                    set_lane<raw_t, VB>(res, l, A::post(fold<A, ALGO, WCAP>(y, W), W));
+                        if (i < W) y[i] = contrib(get_lane<raw_t, VB>(raw[u][i], l));
+                    set_lane<raw_t, VB>(res, l, A::post(fold<A, ALGO, WCAP>(y, W, hop, gmask), W));
                 }
                 if (rs) {
                     store_vec<VB>(static_cast<char*>(P.out[sg.k]) + off - sg.out_lo * EB, res);
@@ -334,12 +381,11 @@ reduce_kernel(const __grid_constant__ ReduceParams P) {
     }
 }
 
-// Instantiate and launch the kernel for one element type.
-template <int DT>
-cudaError_t launch_reduce(const ReduceParams& P, int op, int algo, dim3 grid, cudaStream_t stream) {
-    auto go = [&](auto op_c, auto algo_c) -> cudaError_t {
+// Instantiate and launch the kernel for one element type and one order.
+template <int DT, int ALGO>
+cudaError_t launch_reduce(const ReduceParams& P, int op, dim3 grid, cudaStream_t stream) {
+    auto go = [&](auto op_c) -> cudaError_t {
         constexpr int OP = decltype(op_c)::value;
-        constexpr int ALGO = decltype(algo_c)::value;
         const bool rs = P.mode == MODE_REDUCE_SCATTER;
         switch (reduce_wcap(P.W)) {
             case 2: reduce_kernel<DT, OP, ALGO, 2, 16, reduce_unroll_for(2, false)><<<grid, kThreads, 0, stream>>>(P); break;
@@ -353,16 +399,12 @@ cudaError_t launch_reduce(const ReduceParams& P, int op, int algo, dim3 grid, cu
         }
         return cudaGetLastError();
     };
-    auto with_algo = [&](auto op_c) -> cudaError_t {
-        if (algo == MR_RING) return go(op_c, std::integral_constant<int, MR_RING>{});
-        return go(op_c, std::integral_constant<int, MR_TREE>{});
-    };
     switch (op) {
-        case MR_SUM: return with_algo(std::integral_constant<int, MR_SUM>{});
-        case MR_PROD: return with_algo(std::integral_constant<int, MR_PROD>{});
-        case MR_MIN: return with_algo(std::integral_constant<int, MR_MIN>{});
-        case MR_MAX: return with_algo(std::integral_constant<int, MR_MAX>{});
-        case MR_AVG: return with_algo(std::integral_constant<int, MR_AVG>{});
+        case MR_SUM: return go(std::integral_constant<int, MR_SUM>{});
+        case MR_PROD: return go(std::integral_constant<int, MR_PROD>{});
+        case MR_MIN: return go(std::integral_constant<int, MR_MIN>{});
+        case MR_MAX: return go(std::integral_constant<int, MR_MAX>{});
+        case MR_AVG: return go(std::integral_constant<int, MR_AVG>{});
     }
     return cudaErrorInvalidValue;
 }

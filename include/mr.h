@@ -66,7 +66,7 @@ extern "C" {
 
 typedef enum { MR_FP32 = 0, MR_BF16 = 1, MR_INT32 = 2 } mr_dtype_t;
 typedef enum { MR_SUM = 0, MR_PROD = 1, MR_MIN = 2, MR_MAX = 3, MR_AVG = 4 } mr_op_t;
-typedef enum { MR_RING = 0, MR_TREE = 1 } mr_algo_t;
+typedef enum { MR_RING = 0, MR_TREE = 1, MR_HIER = 2 } mr_algo_t;
 typedef enum {
     MR_OK = 0,
     MR_ERR_INVALID_ARGUMENT = 1, /* W out of [1, 64], NULL or misaligned pointer,
@@ -199,6 +199,42 @@ mr_status_t mr_reduce_scatter_sign_ef(const void* const* grad, void* const* err,
 mr_status_t mr_reduce_scatter_sign_ef_noalloc(const void* const* grad, void* const* err, void* const* recv,
                                               float* scales, int W, size_t N, mr_op_t op, mr_algo_t algo,
                                               void* stream);
+
+/*
+ * All-reduce and reduce-scatter with a choice of accumulation order [HIER]:
+ *   order->algo == MR_RING or MR_TREE: as mr_allreduce / mr_reduce_scatter.
+ *   order->algo == MR_HIER: the ranks form G = W / group groups of `group`
+ *     consecutive ranks (rank a*group + i is local rank i of group a);
+ *     group must divide W.  Element e lies in chunk c of the buffer cut into
+ *     `group` chunks ([EQ2] bounds), and in piece d of chunk c cut into G
+ *     pieces.  Each group first folds its own ranks in local ring order
+ *     c+1, ..., c (the ring reduce-scatter inside a group), then the G group
+ *     totals are folded in group ring order d+1, ..., d (the ring all-reduce
+ *     across groups); the all-gather inside the groups copies.  group == W or
+ *     group == 1 gives exactly MR_RING.
+ *   order->per_hop_rounding == 1 (bf16 only; no effect on fp32 and int32):
+ *     the running total is rounded to bf16 after every combine (and a
+ *     pre-scaled avg contribution as it is read), as when every partial sum
+ *     crosses a wire as bf16 -- NCCL's own bf16 reduction.  0: fp32
+ *     accumulation and one final rounding, as in every other call.
+ * The other arguments, results, aliasing rules and errors are those of
+ * mr_allreduce and mr_reduce_scatter; a NULL order is MR_RING with fp32
+ * accumulation.
+ * [HIER] "Communication Optimization: Gradient Compression, NCCL ..."
+ * (mbrenndoerfer.com): the two-level all-reduce -- local reduce-scatter,
+ * node-level all-reduce of the partial sums, local all-gather; FSDP
+ * collectives 101: NCCL's bf16 reduction accumulates in bf16.
+ */
+typedef struct {
+    mr_algo_t algo;
+    int group;              /* ranks per group, MR_HIER only */
+    int per_hop_rounding;   /* 0 or 1 */
+} mr_order_t;
+
+mr_status_t mr_allreduce_ex(const void* const* send, void* const* recv, int W, size_t N, mr_dtype_t dtype,
+                            mr_op_t op, const mr_order_t* order, void* stream);
+mr_status_t mr_reduce_scatter_ex(const void* const* send, void* const* recv, int W, size_t N, mr_dtype_t dtype,
+                                 mr_op_t op, const mr_order_t* order, void* stream);
 
 /* A static, human-readable name of a status code. */
 const char* mr_status_string(mr_status_t status);

@@ -104,6 +104,9 @@ WORKLOADS = {
     # W=8 DDP bucket sent as 1-bit signs with error feedback: 2^24 fp32
     # gradients Normal(0, 1e-3) and a carried residual Normal(0, 1e-4).
     "sign_ef_fp32_w8": dict(W=8, N=1 << 24, dtype="fp32", dist=("normal", 1e-3), err_dist=("normal", 1e-4)),
+    # W=16 ranks as 2 nodes x 8 GPUs: 2^24 bf16 gradients per rank,
+    # Normal(0, 1e-2), for the two-level (hierarchical) all-reduce order.
+    "hier_bf16_w16": dict(W=16, N=1 << 24, dtype="bf16", dist=("normal", 1e-2)),
     # W=8 size sweep: fp32 Normal(0, 1), N = 2^10, 2^12, ..., 2^26.
     "sweep_fp32_w8": dict(W=8, Ns=[1 << p for p in range(10, 27, 2)], dtype="fp32", dist=("normal", 1.0)),
 }

@@ -96,8 +96,10 @@ def test_argument_errors(mr):
     assert _call_ar(lib, send, recv, 65, 16) == 1
     assert _call_ar(lib, send, recv, 4, 16, dtype=3) == 1
     assert _call_ar(lib, send, recv, 4, 16, op=5) == 1
-    assert _call_ar(lib, send, recv, 4, 16, algo=2) == 1
+    assert _call_ar(lib, send, recv, 4, 16, algo=3) == 1
     assert "algo" in mr.mr_last_error()
+    assert _call_ar(lib, send, recv, 4, 16, algo=2) == 1          # MR_HIER needs the _ex call
+    assert "group" in mr.mr_last_error()
     assert _call_ar(lib, send[:3] + [0], recv, 4, 16) == 1
     assert "send[3]" in mr.mr_last_error()
     assert _call_ar(lib, send, recv[:2] + [recv[2] + 2] + recv[3:], 4, 16) == 1     # misaligned fp32
