@@ -20,7 +20,8 @@ BUILD = os.path.join(ROOT, "_build", "mr")
 LIB = os.path.join(HERE, "libmr.so")
 
 SOURCES = (["api.cu", "all_gather.cu", "rmsnorm_kernel.cu", "sign_ef_kernel.cu", "sign_ef_noalloc.cu"]
-           + [f"reduce_{dt}_{algo}.cu" for dt in ("fp32", "bf16", "int32") for algo in ("ring", "tree", "hier")])
+           + [f"reduce_{dt}_{algo}.cu" for dt in ("fp32", "bf16", "int32") for algo in ("ring", "tree", "hier")]
+           + [f"reduce_bf16_{algo}_hop.cu" for algo in ("ring", "tree", "hier")])
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ARCH + ["-O3", "-lineinfo", "-std=c++17", "-fmad=false", "-Xcompiler", "-fPIC,-O2",
                 "-I", INCLUDE, "-I", CSRC]

@@ -229,6 +229,10 @@ cudaError_t launch_reduce(mr_dtype_t dtype, const mr::ReduceParams& P, mr_op_t o
                  : algo == MR_TREE ? mr::launch_reduce_fp32_tree(P, op, grid, s)
                                    : mr::launch_reduce_fp32_hier(P, op, grid, s);
         case MR_BF16:
+            if (P.hop)
+                return algo == MR_RING ? mr::launch_reduce_bf16_ring_hop(P, op, grid, s)
+                     : algo == MR_TREE ? mr::launch_reduce_bf16_tree_hop(P, op, grid, s)
+                                       : mr::launch_reduce_bf16_hier_hop(P, op, grid, s);
             return algo == MR_RING ? mr::launch_reduce_bf16_ring(P, op, grid, s)
                  : algo == MR_TREE ? mr::launch_reduce_bf16_tree(P, op, grid, s)
                                    : mr::launch_reduce_bf16_hier(P, op, grid, s);

@@ -124,6 +124,9 @@ MR_DECLARE_REDUCE(fp32, hier)
 MR_DECLARE_REDUCE(bf16, ring)
 MR_DECLARE_REDUCE(bf16, tree)
 MR_DECLARE_REDUCE(bf16, hier)
+MR_DECLARE_REDUCE(bf16, ring_hop)
+MR_DECLARE_REDUCE(bf16, tree_hop)
+MR_DECLARE_REDUCE(bf16, hier_hop)
 MR_DECLARE_REDUCE(int32, ring)
 MR_DECLARE_REDUCE(int32, tree)
 MR_DECLARE_REDUCE(int32, hier)

@@ -1,12 +1,12 @@
 // reduce_bf16_ring.cu -- the fused all-reduce / reduce-scatter kernels for
-// bf16 buffers in the ring order (one translation unit per element type and
-// order keeps the build parallel).
+// bf16 buffers in the ring order (one translation unit per element
+// type and order keeps the build parallel).
 #include "reduce_kernel.cuh"
 
 namespace mr {
 
 cudaError_t launch_reduce_bf16_ring(const ReduceParams& P, int op, dim3 grid, cudaStream_t s) {
-    return launch_reduce<MR_BF16, MR_RING>(P, op, grid, s);
+    return launch_reduce<MR_BF16, MR_RING, false>(P, op, grid, s);
 }
 
 }  // namespace mr

@@ -1,12 +1,12 @@
 // reduce_fp32_hier.cu -- the fused all-reduce / reduce-scatter kernels for
-// fp32 buffers in the hier order (one translation unit per element type and
-// order keeps the build parallel).
+// fp32 buffers in the hier order (one translation unit per element
+// type and order keeps the build parallel).
 #include "reduce_kernel.cuh"
 
 namespace mr {
 
 cudaError_t launch_reduce_fp32_hier(const ReduceParams& P, int op, dim3 grid, cudaStream_t s) {
-    return launch_reduce<MR_FP32, MR_HIER>(P, op, grid, s);
+    return launch_reduce<MR_FP32, MR_HIER, false>(P, op, grid, s);
 }
 
 }  // namespace mr

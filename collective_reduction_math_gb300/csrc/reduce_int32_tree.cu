@@ -1,12 +1,12 @@
 // reduce_int32_tree.cu -- the fused all-reduce / reduce-scatter kernels for
-// int32 buffers in the tree order (one translation unit per element type and
-// order keeps the build parallel).
+// int32 buffers in the tree order (one translation unit per element
+// type and order keeps the build parallel).
 #include "reduce_kernel.cuh"
 
 namespace mr {
 
 cudaError_t launch_reduce_int32_tree(const ReduceParams& P, int op, dim3 grid, cudaStream_t s) {
-    return launch_reduce<MR_INT32, MR_TREE>(P, op, grid, s);
+    return launch_reduce<MR_INT32, MR_TREE, false>(P, op, grid, s);
 }
 
 }  // namespace mr

@@ -231,6 +231,70 @@ template <class raw_t, int VB> __device__ __forceinline__ void set_lane(Vec<VB>&
     }
 }
 
+// The vector path's fold: all LANES elements of one vector at once.  The
+// hierarchical order, and the ring on 8-lane (bf16) vectors, run positions
+// outer and lanes inner, so each position's (warp-uniform) decisions --
+// inside W, start of a group, per-hop rounding -- are taken once per vector
+// rather than once per lane; the tree, and the ring on 4-lane vectors, run
+// lane by lane (measured faster for fp32 on GB300).  contrib(x) widens,
+// pre-scales and (per-hop) rounds one raw contribution.
+template <class A, int ALGO, int WCAP, int VB, int LANES, class Contrib>
+__device__ __forceinline__ void fold_lanes(const Vec<VB> (&raw)[WCAP], int W, uint64_t gmask, bool hop,
+                                           Contrib contrib, typename A::acc_t (&out)[LANES]) {
+    using acc_t = typename A::acc_t;
+    using raw_t = typename A::raw_t;
+    if constexpr (ALGO == MR_TREE || (ALGO == MR_RING && LANES <= 4)) {
+#pragma unroll
+        for (int l = 0; l < LANES; ++l) {
+            acc_t y[WCAP];
+#pragma unroll
+            for (int i = 0; i < WCAP; ++i)
+                if (i < W) y[i] = contrib(get_lane<raw_t, VB>(raw[i], l));
+            if constexpr (ALGO == MR_TREE) out[l] = fold_tree<A, WCAP>(y, W, hop);
+            else out[l] = fold_ring<A, WCAP>(y, W, hop);
+        }
+    } else if constexpr (ALGO == MR_RING) {
+#pragma unroll
+        for (int l = 0; l < LANES; ++l) out[l] = contrib(get_lane<raw_t, VB>(raw[0], l));
+#pragma unroll
+        for (int i = 1; i < WCAP; ++i) {
+            if (i < W) {
+#pragma unroll
+                for (int l = 0; l < LANES; ++l) out[l] = comb<A>(out[l], contrib(get_lane<raw_t, VB>(raw[i], l)), hop);
+            }
+        }
+    } else {
+        acc_t total[LANES];
+        bool have_total = false;
+#pragma unroll
+        for (int l = 0; l < LANES; ++l) out[l] = contrib(get_lane<raw_t, VB>(raw[0], l));   // the running group part
+#pragma unroll
+        for (int i = 1; i < WCAP; ++i) {
+            if (i < W) {
+                if ((gmask >> i) & 1u) {
+                    if (have_total) {
+#pragma unroll
+                        for (int l = 0; l < LANES; ++l) total[l] = comb<A>(total[l], out[l], hop);
+                    } else {
+#pragma unroll
+                        for (int l = 0; l < LANES; ++l) total[l] = out[l];
+                    }
+                    have_total = true;
+#pragma unroll
+                    for (int l = 0; l < LANES; ++l) out[l] = contrib(get_lane<raw_t, VB>(raw[i], l));
+                } else {
+#pragma unroll
+                    for (int l = 0; l < LANES; ++l) out[l] = comb<A>(out[l], contrib(get_lane<raw_t, VB>(raw[i], l)), hop);
+                }
+            }
+        }
+        if (have_total) {
+#pragma unroll
+            for (int l = 0; l < LANES; ++l) out[l] = comb<A>(total[l], out[l], hop);
+        }
+    }
+}
+
 // ---------------------------------------------------------------------------
 // The kernel
 // ---------------------------------------------------------------------------
@@ -243,7 +307,7 @@ __device__ __forceinline__ int order_rank(int W, const Segment& sg, int i, int g
     else return hier_rank(W, group, sg.hc, sg.hd, i);
 }
 
-template <int DT, int OP, int ALGO, int WCAP, int VB, int U>
+template <int DT, int OP, int ALGO, int WCAP, int VB, int U, bool HOP>
 __global__ void __launch_bounds__(kThreads, reduce_blocks_per_sm(WCAP, U))
 reduce_kernel(const __grid_constant__ ReduceParams P) {
     using A = Arith<DT, OP>;
@@ -255,7 +319,7 @@ reduce_kernel(const __grid_constant__ ReduceParams P) {
     const int W = P.W;
     const float s = P.scale;
     const bool rs = (P.mode == MODE_REDUCE_SCATTER);
-    const bool hop = DT == MR_BF16 && P.hop;
+    constexpr bool hop = DT == MR_BF16 && HOP;
     const uint64_t gmask = P.gmask;
     // a contribution as read: widened, pre-scaled, and for per-hop bf16 rounded
     auto contrib = [&](raw_t x) -> acc_t {
@@ -338,14 +402,10 @@ reduce_kernel(const __grid_constant__ ReduceParams P) {
                 if (v >= vb) break;
                 const uint64_t off = v * VB;
                 Vec<VB> res;
+                acc_t r[LANES];
+                fold_lanes<A, ALGO, WCAP, VB, LANES>(raw[u], W, gmask, hop, contrib, r);
 #pragma unroll
-                for (int l = 0; l < LANES; ++l) {
-                    acc_t y[WCAP];
-#pragma unroll
-                    for (int i = 0; i < WCAP; ++i)
-                        if (i < W) y[i] = contrib(get_lane<raw_t, VB>(raw[u][i], l));
-                    set_lane<raw_t, VB>(res, l, A::post(fold<A, ALGO, WCAP>(y, W, hop, gmask), W));
-                }
+                for (int l = 0; l < LANES; ++l) set_lane<raw_t, VB>(res, l, A::post(r[l], W));
                 if (rs) {
                     store_vec<VB>(static_cast<char*>(P.out[sg.k]) + off - sg.out_lo * EB, res);
                 } else {
@@ -382,20 +442,20 @@ reduce_kernel(const __grid_constant__ ReduceParams P) {
 }
 
 // Instantiate and launch the kernel for one element type and one order.
-template <int DT, int ALGO>
+template <int DT, int ALGO, bool HOP>
 cudaError_t launch_reduce(const ReduceParams& P, int op, dim3 grid, cudaStream_t stream) {
     auto go = [&](auto op_c) -> cudaError_t {
         constexpr int OP = decltype(op_c)::value;
         const bool rs = P.mode == MODE_REDUCE_SCATTER;
         switch (reduce_wcap(P.W)) {
-            case 2: reduce_kernel<DT, OP, ALGO, 2, 16, reduce_unroll_for(2, false)><<<grid, kThreads, 0, stream>>>(P); break;
-            case 4: reduce_kernel<DT, OP, ALGO, 4, 16, reduce_unroll_for(4, false)><<<grid, kThreads, 0, stream>>>(P); break;
+            case 2: reduce_kernel<DT, OP, ALGO, 2, 16, reduce_unroll_for(2, false), HOP><<<grid, kThreads, 0, stream>>>(P); break;
+            case 4: reduce_kernel<DT, OP, ALGO, 4, 16, reduce_unroll_for(4, false), HOP><<<grid, kThreads, 0, stream>>>(P); break;
             case 8:
-                if (rs) reduce_kernel<DT, OP, ALGO, 8, 16, reduce_unroll_for(8, true)><<<grid, kThreads, 0, stream>>>(P);
-                else reduce_kernel<DT, OP, ALGO, 8, 16, reduce_unroll_for(8, false)><<<grid, kThreads, 0, stream>>>(P);
+                if (rs) reduce_kernel<DT, OP, ALGO, 8, 16, reduce_unroll_for(8, true), HOP><<<grid, kThreads, 0, stream>>>(P);
+                else reduce_kernel<DT, OP, ALGO, 8, 16, reduce_unroll_for(8, false), HOP><<<grid, kThreads, 0, stream>>>(P);
                 break;
-            case 16: reduce_kernel<DT, OP, ALGO, 16, 16, reduce_unroll_for(16, false)><<<grid, kThreads, 0, stream>>>(P); break;
-            default: reduce_kernel<DT, OP, ALGO, 64, 4, reduce_unroll_for(64, false)><<<grid, kThreads, 0, stream>>>(P); break;
+            case 16: reduce_kernel<DT, OP, ALGO, 16, 16, reduce_unroll_for(16, false), HOP><<<grid, kThreads, 0, stream>>>(P); break;
+            default: reduce_kernel<DT, OP, ALGO, 64, 4, reduce_unroll_for(64, false), HOP><<<grid, kThreads, 0, stream>>>(P); break;
         }
         return cudaGetLastError();
     };
