@@ -56,7 +56,7 @@ def parse_args():
                    default=None,
                    help="the collective timed as one step (default: the workload's own)")
     p.add_argument("--op", default=None)
-    p.add_argument("--algo", default="ring", choices=["ring", "tree", "hier"])
+    p.add_argument("--algo", default="ring", choices=["ring", "tree", "hier", "auto"])
     p.add_argument("--group", type=int, default=None, help="ranks per group for --algo hier")
     p.add_argument("--per-hop", action="store_true", help="round a bf16 running total to bf16 after every hop")
     p.add_argument("--n", type=int, default=None, help="elements per rank (sweep workload)")
@@ -283,7 +283,8 @@ def extras(mr, torch, dev):
         xs = [torch.from_numpy(h).to(dev) for h in host]
         ys = [torch.empty_like(x) for x in xs]
         row = {"N_per_rank": N, "bytes_per_rank": N * 4}
-        for algo in ("ring", "tree"):
+        row["auto_picks"] = mr.mr_plan_auto(W, N, "fp32")[0]
+        for algo in ("ring", "tree", "auto"):
             def call():
                 mr.mr_allreduce(xs, ys, op="sum", algo=algo)
             for _ in range(5):

@@ -20,7 +20,7 @@ __all__ = [
     "mr_allreduce", "mr_reduce_scatter", "mr_all_gather", "mr_allreduce_ex", "mr_reduce_scatter_ex", "mr_allreduce_rmsnorm", "mr_allreduce_sign_ef",
     "mr_reduce_scatter_sign_ef", "mr_reduce_scatter_sign_ef_noalloc", "mr_sign_ef_workspace_bytes",
     "mr_status_string", "mr_last_error",
-    "mr_allreduce_ptrs", "mr_plan_ring_order", "mr_plan_tree", "mr_chunk_lo", "mr_launch_count", "MRError",
+    "mr_allreduce_ptrs", "mr_plan_auto", "mr_plan_ring_order", "mr_plan_tree", "mr_chunk_lo", "mr_launch_count", "MRError",
     "load", "LIB_PATH",
     "DTYPES", "OPS", "ALGOS", "MAX_RANKS",
 ]
@@ -29,7 +29,7 @@ LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libmr.so")
 MAX_RANKS = 64
 DTYPES = {"fp32": 0, "bf16": 1, "int32": 2}
 OPS = {"sum": 0, "prod": 1, "min": 2, "max": 3, "avg": 4}
-ALGOS = {"ring": 0, "tree": 1, "hier": 2}
+ALGOS = {"ring": 0, "tree": 1, "hier": 2, "auto": 3}
 STATUS = {0: "MR_OK", 1: "MR_ERR_INVALID_ARGUMENT", 2: "MR_ERR_UNSUPPORTED", 3: "MR_ERR_ALIAS", 4: "MR_ERR_CUDA"}
 
 _lib = None
@@ -86,6 +86,8 @@ def load():
     L.mr_plan_tree.restype = i
     L.mr_chunk_lo.argtypes = [i, sz, i]
     L.mr_chunk_lo.restype = sz
+    L.mr_plan_auto.argtypes = [i, sz, i, i, ctypes.POINTER(ctypes.c_int), ctypes.POINTER(ctypes.c_double)]
+    L.mr_plan_auto.restype = i
     L.mr_launch_count.argtypes = []
     L.mr_launch_count.restype = ctypes.c_ulonglong
     _lib = L
@@ -313,6 +315,16 @@ def mr_plan_tree(W: int, which: int):
         _raise(st)
     kids = [[c for c in child[2 * r:2 * r + 2] if c >= 0] for r in range(W)]
     return root.value, list(parent), kids
+
+
+def mr_plan_auto(W: int, N: int, dtype: str, reduce_scatter: bool = False):
+    """The order MR_AUTO picks for a call, and the cost model's time (us)."""
+    a = ctypes.c_int()
+    t = ctypes.c_double()
+    st = load().mr_plan_auto(W, N, _code(DTYPES, dtype, "dtype"), int(reduce_scatter), ctypes.byref(a), ctypes.byref(t))
+    if st:
+        _raise(st)
+    return {0: "ring", 1: "tree"}[a.value], t.value
 
 
 def mr_chunk_lo(W: int, N: int, k: int) -> int:

@@ -40,12 +40,46 @@ mr_status_t fail(mr_status_t st, const char* fmt, ...) {
 }
 
 size_t elem_bytes(mr_dtype_t dt) { return dt == MR_BF16 ? 2u : 4u; }
+
+// The alpha-beta cost model of the orders (t = alpha + bytes / beta), fitted
+// on GB300 per element type, rank count and order.
+struct CostRow {
+    int dtype, W, algo;
+    double alpha_us, beta_gbs;
+};
+const CostRow kCostModel[] = {
+#include "cost_model.inc"
+};
+
+double model_us(mr_dtype_t dtype, int W, mr_algo_t algo, double bytes) {
+    // the row of the smallest tabulated W that covers W, else of the largest
+    const CostRow* row = nullptr;
+    const CostRow* largest = nullptr;
+    for (const CostRow& c : kCostModel) {
+        if (c.dtype != (int)dtype || c.algo != (int)algo) continue;
+        if (c.W >= W && (!row || c.W < row->W)) row = &c;
+        if (!largest || c.W > largest->W) largest = &c;
+    }
+    if (!row) row = largest;
+    if (!row) return 1e30;
+    return row->alpha_us + bytes / (row->beta_gbs * 1e3);
+}
+
+// MR_AUTO: the order with the smaller modelled time (ring on a tie).
+mr_algo_t resolve_auto(mr_dtype_t dtype, int W, size_t N, bool rs, double* predicted) {
+    const double b = (double)elem_bytes(dtype) * (double)N * (rs ? (double)(W + 1) : 2.0 * W);
+    const double tr = model_us(dtype, W, MR_RING, b), tt = model_us(dtype, W, MR_TREE, b);
+    if (predicted) *predicted = tt < tr ? tt : tr;
+    return tt < tr ? MR_TREE : MR_RING;
+}
 const char* dtype_name(mr_dtype_t dt) { return dt == MR_FP32 ? "fp32" : dt == MR_BF16 ? "bf16" : "int32"; }
 const char* op_name(mr_op_t op) {
     static const char* n[] = {"sum", "prod", "min", "max", "avg"};
     return n[op];
 }
-const char* algo_name(mr_algo_t a) { return a == MR_RING ? "ring" : a == MR_TREE ? "tree" : "hier"; }
+const char* algo_name(mr_algo_t a) {
+    return a == MR_RING ? "ring" : a == MR_TREE ? "tree" : a == MR_HIER ? "hier" : "auto";
+}
 
 // Streaming multiprocessors of the current device (cached per device).
 int sm_count() {
@@ -91,7 +125,8 @@ mr_status_t check_op_algo(mr_op_t op, mr_algo_t algo) {
     if (op < MR_SUM || op > MR_AVG) return fail(MR_ERR_INVALID_ARGUMENT, "unknown op %d", (int)op);
     if (algo == MR_HIER)
         return fail(MR_ERR_INVALID_ARGUMENT, "MR_HIER needs a group size: use mr_allreduce_ex / mr_reduce_scatter_ex");
-    if (algo != MR_RING && algo != MR_TREE) return fail(MR_ERR_INVALID_ARGUMENT, "unknown algo %d", (int)algo);
+    if (algo != MR_RING && algo != MR_TREE && algo != MR_AUTO)
+        return fail(MR_ERR_INVALID_ARGUMENT, "unknown algo %d", (int)algo);
     return MR_OK;
 }
 
@@ -246,6 +281,9 @@ cudaError_t launch_reduce(mr_dtype_t dtype, const mr::ReduceParams& P, mr_op_t o
 
 mr_status_t run_reduce(const char* what, int mode, const void* const* send, void* const* recv, int W, size_t N,
                        mr_dtype_t dtype, mr_op_t op, mr_algo_t algo, void* stream, int group = 0, int hop = 0) {
+    const bool is_auto = algo == MR_AUTO;
+    double predicted = 0.0;
+    if (is_auto) algo = resolve_auto(dtype, W, N, mode == mr::MODE_REDUCE_SCATTER, &predicted);
     mr::ReduceParams P;
     for (int r = 0; r < W; ++r) {
         P.in[r] = send[r];
@@ -272,6 +310,8 @@ mr_status_t run_reduce(const char* what, int mode, const void* const* send, void
     if (err != cudaSuccess)
         return fail(MR_ERR_CUDA, "%s launch failed: %s", what, cudaGetErrorString(err));
     g_launches.fetch_add(1, std::memory_order_relaxed);
+    if (debug_level() > 0 && is_auto)
+        fprintf(stderr, "[mr] %s auto -> %s (model %.2f us)\n", what, algo_name(algo), predicted);
     if (debug_level() > 0)
         fprintf(stderr, "[mr] %s dtype=%s op=%s algo=%s group=%d per_hop=%d W=%d N=%zu segments=%d tiles=%llu "
                 "vector=%d grid=%u threads=%d\n",
@@ -374,7 +414,7 @@ static mr_status_t check_order(const mr_order_t* order, int W, mr_algo_t* algo, 
     *group = W;
     *hop = 0;
     if (!order) return MR_OK;
-    if (order->algo != MR_RING && order->algo != MR_TREE && order->algo != MR_HIER)
+    if (order->algo != MR_RING && order->algo != MR_TREE && order->algo != MR_HIER && order->algo != MR_AUTO)
         return fail(MR_ERR_INVALID_ARGUMENT, "unknown algo %d", (int)order->algo);
     if (order->per_hop_rounding != 0 && order->per_hop_rounding != 1)
         return fail(MR_ERR_INVALID_ARGUMENT, "per_hop_rounding must be 0 or 1");
@@ -462,6 +502,7 @@ mr_status_t mr_allreduce_rmsnorm(const void* const* send, void* const* recv, int
     });
     if (st != MR_OK) return st;
 
+    if (algo == MR_AUTO) algo = resolve_auto(dtype, W, N, false, nullptr);
     mr::NormParams P;
     for (int r = 0; r < W; ++r) {
         P.in[r] = send[r];
@@ -546,6 +587,7 @@ static mr_status_t run_sign_ef(const char* what, int mode, const void* const* gr
     });
     if (st != MR_OK) return st;
 
+    if (algo == MR_AUTO) algo = resolve_auto(MR_FP32, W, N, mode == mr::MODE_REDUCE_SCATTER, nullptr);
     mr::SignParams P;
     for (int r = 0; r < W; ++r) {
         P.grad[r] = grad[r];
@@ -649,6 +691,15 @@ mr_status_t mr_plan_tree(int W, int which, int* parent, int* child, int* root) {
         if (up >= 0) child[2 * r + n++] = mr::tree_rank(W, t, up);
     }
     *root = mr::tree_rank(W, t, 0);
+    return MR_OK;
+}
+
+mr_status_t mr_plan_auto(int W, size_t N, mr_dtype_t dtype, int reduce_scatter, mr_algo_t* algo,
+                         double* predicted_us) {
+    g_last_error.clear();
+    if (W < 1 || W > MR_MAX_RANKS || !algo || (dtype != MR_FP32 && dtype != MR_BF16 && dtype != MR_INT32))
+        return fail(MR_ERR_INVALID_ARGUMENT, "mr_plan_auto: bad W, dtype or algo pointer");
+    *algo = resolve_auto(dtype, W, N, reduce_scatter != 0, predicted_us);
     return MR_OK;
 }
 

@@ -66,7 +66,7 @@ extern "C" {
 
 typedef enum { MR_FP32 = 0, MR_BF16 = 1, MR_INT32 = 2 } mr_dtype_t;
 typedef enum { MR_SUM = 0, MR_PROD = 1, MR_MIN = 2, MR_MAX = 3, MR_AVG = 4 } mr_op_t;
-typedef enum { MR_RING = 0, MR_TREE = 1, MR_HIER = 2 } mr_algo_t;
+typedef enum { MR_RING = 0, MR_TREE = 1, MR_HIER = 2, MR_AUTO = 3 } mr_algo_t;
 typedef enum {
     MR_OK = 0,
     MR_ERR_INVALID_ARGUMENT = 1, /* W out of [1, 64], NULL or misaligned pointer,
@@ -242,6 +242,25 @@ const char* mr_status_string(mr_status_t status);
 /* Detail of the last non-OK status returned on the calling thread ("" if none).
  * The string is owned by the library and valid until the thread's next call. */
 const char* mr_last_error(void);
+
+/*
+ * MR_AUTO [COST]: wherever an algo is taken (except inside mr_order_t's
+ * MR_HIER), MR_AUTO picks MR_RING or MR_TREE per call as the argmin of the
+ * alpha-beta model  t = alpha + bytes / beta  of each order, with alpha and
+ * beta fitted on GB300 per element type and rank count (the table the library
+ * is built with; collective_reduction_math_gb300/tune_cost_model.py refits it
+ * on another GPU).  bytes is the call's HBM traffic.  The choice depends only
+ * on (dtype, W, N, call), so results are reproducible; they equal those of
+ * the order chosen, which mr_plan_auto reports.  Integer ops and min / max
+ * give the same result in either order.
+ *   mr_plan_auto: *algo receives MR_RING or MR_TREE and *predicted_us (if not
+ *   NULL) the model's time; reduce_scatter = 0 for all-reduce traffic
+ *   (2 W N b bytes), 1 for reduce-scatter ((W + 1) N b).
+ * [COST] post on NCCL all-reduce, "How NCCL picks: a cost model, not a
+ * threshold": time = lat * latCount + nBytes / bw, argmin per call.
+ */
+mr_status_t mr_plan_auto(int W, size_t N, mr_dtype_t dtype, int reduce_scatter, mr_algo_t* algo,
+                         double* predicted_us);
 
 /*
  * Planner queries (host only; no GPU needed).  They expose the orders the

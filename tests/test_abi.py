@@ -96,7 +96,7 @@ def test_argument_errors(mr):
     assert _call_ar(lib, send, recv, 65, 16) == 1
     assert _call_ar(lib, send, recv, 4, 16, dtype=3) == 1
     assert _call_ar(lib, send, recv, 4, 16, op=5) == 1
-    assert _call_ar(lib, send, recv, 4, 16, algo=3) == 1
+    assert _call_ar(lib, send, recv, 4, 16, algo=4) == 1
     assert "algo" in mr.mr_last_error()
     assert _call_ar(lib, send, recv, 4, 16, algo=2) == 1          # MR_HIER needs the _ex call
     assert "group" in mr.mr_last_error()
@@ -144,3 +144,38 @@ def test_valid_call_without_gpu_reports_cuda_error(mr):
     recv = [base + (1 << 30) + r * 4096 for r in range(2)]
     assert _call_ar(lib, send, recv, 2, 1024) == 4
     assert "launch failed" in mr.mr_last_error()
+
+
+def _cost_table():
+    rows = []
+    path = os.path.join(ROOT, "collective_reduction_math_gb300", "csrc", "cost_model.inc")
+    for line in open(path):
+        line = line.strip()
+        if line.startswith("{"):
+            d, w, a, alpha, beta = [x.strip() for x in line.strip("{},").split(",")]
+            rows.append((int(d), int(w), int(a), float(alpha), float(beta)))
+    return rows
+
+
+def test_auto_is_the_cost_model_argmin(mr):
+    """MR_AUTO picks, per call, the order with the smaller alpha + bytes/beta
+    of the table the library was built with (recomputed here from the table)."""
+    rows = _cost_table()
+    assert len(rows) == 3 * 6 * 2
+    codes = {"fp32": 0, "bf16": 1, "int32": 2}
+    sizes = {"fp32": 4, "bf16": 2, "int32": 4}
+    for dtype in codes:
+        for W in (1, 2, 3, 8, 13, 16, 33, 64):
+            for N in (1 << 10, 1 << 16, 1 << 20, 1 << 24):
+                for rs in (False, True):
+                    b = sizes[dtype] * N * ((W + 1) if rs else 2 * W)
+                    t = {}
+                    for a in (0, 1):
+                        cand = [r for r in rows if r[0] == codes[dtype] and r[2] == a]
+                        cover = [r for r in cand if r[1] >= W]
+                        row = min(cover, key=lambda r: r[1]) if cover else max(cand, key=lambda r: r[1])
+                        t[a] = row[3] + b / (row[4] * 1e3)
+                    want = "tree" if t[1] < t[0] else "ring"
+                    algo, pred = mr.mr_plan_auto(W, N, dtype, rs)
+                    assert algo == want, (dtype, W, N, rs)
+                    assert abs(pred - min(t.values())) <= 1e-9 * max(1.0, pred)

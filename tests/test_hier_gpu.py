@@ -91,3 +91,30 @@ def test_hier_errors(mr):
     with pytest.raises(mr.MRError) as e:
         mr.mr_allreduce(xs, ys, algo="hier")                   # the plain call has no group
     assert e.value.status == 1
+
+
+@pytest.mark.parametrize("dtype", ["fp32", "bf16", "int32"])
+def test_auto_equals_the_planned_order(mr, dtype):
+    """MR_AUTO gives exactly the result of the order mr_plan_auto names."""
+    import oracle
+    import torch
+    for W, N in ((2, 4096), (8, 1 << 16), (16, 1 << 14), (33, 3000), (8, 1 << 22)):
+        host = synth.random_values(720 + W, W, N, dtype)
+        xs = [to_device(h, dtype) for h in host]
+        planned, _ = mr.mr_plan_auto(W, N, dtype)
+        ys = [torch.empty_like(x) for x in xs]
+        mr.mr_allreduce(xs, ys, op="avg", algo="auto")
+        torch.cuda.synchronize()
+        want = oracle.allreduce(dtype, "avg", planned, host)
+        for j, y in enumerate(ys):
+            assert_same(y.view(torch.int16).cpu().numpy().view(np.uint16) if dtype == "bf16" else y.cpu().numpy(),
+                        want, f"auto ({planned}) {dtype} W={W} N={N} rank {j}")
+        if N % W == 0:
+            planned_rs, _ = mr.mr_plan_auto(W, N, dtype, reduce_scatter=True)
+            sh = [torch.empty(N // W, dtype=xs[0].dtype, device="cuda") for _ in range(W)]
+            mr.mr_reduce_scatter(xs, sh, op="sum", algo="auto")
+            torch.cuda.synchronize()
+            want_rs = oracle.reduce_scatter(dtype, "sum", planned_rs, host)
+            for k, t in enumerate(sh):
+                got = t.view(torch.int16).cpu().numpy().view(np.uint16) if dtype == "bf16" else t.cpu().numpy()
+                assert_same(got, want_rs[k], f"auto rs ({planned_rs}) {dtype} W={W} shard {k}")
