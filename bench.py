@@ -182,6 +182,21 @@ class ClockSampler:
 # the reference arm: the CPU oracle on the host cores
 # ---------------------------------------------------------------------------
 
+def slowest_rank_ms(ms: float, dist, device) -> float:
+    """The timed region's length on the slowest rank (every rank gets it)."""
+    if dist is None:
+        return ms
+    import torch
+    t = torch.tensor([ms], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_gbs(world: int, bytes_per_step: int, steps: int, ms: float) -> float:
+    """Whole-job throughput: every replica's bytes over the slowest rank's time."""
+    return world * bytes_per_step * steps / (ms * 1e-3) / 1e9
+
+
 def run_reference(args):
     if int(os.environ.get("RANK", "0")) != 0:
         return 0
@@ -551,11 +566,8 @@ def run_mine(args):
     clocks = sampler.stop()
     total_ms = t_start.elapsed_time(t_end)
     kern_ms = statistics.mean(a.elapsed_time(b) for a, b in per) / per_replay
-    if dist:
-        t = torch.tensor([total_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        total_ms = float(t.item())
-    value = world * bytes_step * K / (total_ms * 1e-3) / 1e9
+    total_ms = slowest_rank_ms(total_ms, dist, dev)
+    value = job_gbs(world, bytes_step, K, total_ms)
 
     peak, peak_src = peaks()
     achieved = bytes_step / (kern_ms * 1e-3) / 1e9
