@@ -109,7 +109,9 @@ struct GatherParams {
 // vector per W loads, and at W = 8 runs faster with two vectors per thread at
 // 2 CTAs per SM (measured on GB300: 6.8 against 5.8 TB/s).
 constexpr int reduce_wcap(int W) { return W <= 2 ? 2 : W <= 4 ? 4 : W <= 8 ? 8 : W <= 16 ? 16 : 64; }
-constexpr int reduce_vector_bytes(int W) { return W <= 16 ? 16 : 4; }
+// Above 16 ranks the tree keeps all W values in registers and so narrows its
+// vectors to 4 bytes; the left-fold orders fold in batches of 8 and keep 16.
+constexpr int reduce_vector_bytes(int W, int algo) { return (W <= 16 || algo != MR_TREE) ? 16 : 4; }
 constexpr int reduce_unroll_for(int wcap, bool rs) {
     return wcap == 2 ? 4 : wcap == 4 ? 2 : (wcap == 8 && rs) ? 2 : 1;
 }

@@ -330,6 +330,7 @@ reduce_kernel(const __grid_constant__ ReduceParams P) {
     // Input pointers in the current segment's accumulation order: in
     // registers for up to 16 ranks, in a shared-memory table beyond that.
     constexpr bool kTable = WCAP > 16;
+    constexpr bool kBatched = WCAP > 16 && ALGO != MR_TREE;
     __shared__ const char* table[kTable ? WCAP : 1];
     const char* src[kTable ? 1 : WCAP];
     int cur = -1;
@@ -385,6 +386,62 @@ reduce_kernel(const __grid_constant__ ReduceParams P) {
             const Segment& sg = P.seg[seg];
             const uint64_t va = (sg.lo + LANES - 1) / LANES, vb = sg.hi / LANES;
             const uint64_t v0 = va + local * kTile + threadIdx.x;
+            if constexpr (kBatched) {
+                // More than 16 ranks in a left-fold order (ring, hierarchical):
+                // the ranks come in batches of 8 (8 independent 16-byte loads
+                // in flight, as at W = 8) and the fold's state -- the running
+                // group part and the total of the groups so far -- carries
+                // from batch to batch.  Same order, same operations.
+                if (v0 < vb) {
+                    const uint64_t off = v0 * VB;
+                    acc_t part[LANES], total[LANES];
+                    bool have_total = false;
+                    for (int b0 = 0; b0 < W; b0 += 8) {
+                        Vec<VB> raw[8];
+#pragma unroll
+                        for (int i = 0; i < 8; ++i)
+                            if (b0 + i < W) raw[i] = load_vec<VB>(input(b0 + i) + off);
+#pragma unroll
+                        for (int i = 0; i < 8; ++i) {
+                            const int p = b0 + i;
+                            if (p >= W) break;
+                            if (p == 0) {
+#pragma unroll
+                                for (int l = 0; l < LANES; ++l) part[l] = contrib(get_lane<raw_t, VB>(raw[i], l));
+                            } else if (ALGO == MR_HIER && ((gmask >> p) & 1u)) {
+                                if (have_total) {
+#pragma unroll
+                                    for (int l = 0; l < LANES; ++l) total[l] = comb<A>(total[l], part[l], hop);
+                                } else {
+#pragma unroll
+                                    for (int l = 0; l < LANES; ++l) total[l] = part[l];
+                                }
+                                have_total = true;
+#pragma unroll
+                                for (int l = 0; l < LANES; ++l) part[l] = contrib(get_lane<raw_t, VB>(raw[i], l));
+                            } else {
+#pragma unroll
+                                for (int l = 0; l < LANES; ++l)
+                                    part[l] = comb<A>(part[l], contrib(get_lane<raw_t, VB>(raw[i], l)), hop);
+                            }
+                        }
+                    }
+                    if (have_total) {
+#pragma unroll
+                        for (int l = 0; l < LANES; ++l) part[l] = comb<A>(total[l], part[l], hop);
+                    }
+                    Vec<VB> res;
+#pragma unroll
+                    for (int l = 0; l < LANES; ++l) set_lane<raw_t, VB>(res, l, A::post(part[l], W));
+                    if (rs) {
+                        store_vec<VB>(static_cast<char*>(P.out[sg.k]) + off - sg.out_lo * EB, res);
+                    } else {
+#pragma unroll 8
+                        for (int j = 0; j < W; ++j) store_vec<VB>(static_cast<char*>(P.out[j]) + off, res);
+                    }
+                }
+                continue;
+            }
             // U*W independent 16-byte loads in flight before the first fold.
             Vec<VB> raw[U][WCAP];
 #pragma unroll
@@ -455,7 +512,10 @@ cudaError_t launch_reduce(const ReduceParams& P, int op, dim3 grid, cudaStream_t
                 else reduce_kernel<DT, OP, ALGO, 8, 16, reduce_unroll_for(8, false), HOP><<<grid, kThreads, 0, stream>>>(P);
                 break;
             case 16: reduce_kernel<DT, OP, ALGO, 16, 16, reduce_unroll_for(16, false), HOP><<<grid, kThreads, 0, stream>>>(P); break;
-            default: reduce_kernel<DT, OP, ALGO, 64, 4, reduce_unroll_for(64, false), HOP><<<grid, kThreads, 0, stream>>>(P); break;
+            default:
+                reduce_kernel<DT, OP, ALGO, 64, reduce_vector_bytes(64, ALGO), reduce_unroll_for(64, false), HOP>
+                    <<<grid, kThreads, 0, stream>>>(P);
+                break;
         }
         return cudaGetLastError();
     };
