@@ -160,3 +160,17 @@ def workload_sign_operands(name: str, seed: int = 0, N: int | None = None):
     n = N if N is not None else w["N"]
     return (draw(w["dist"], seed, w["W"], n, w["dtype"], TAG_GRAD),
             draw(w["err_dist"], seed, w["W"], n, w["dtype"], TAG_ERR))
+
+
+def device_normal(seed: int, W: int, N: int, dtype: str, device="cuda", tag: int = TAG_GRAD):
+    """W rank buffers of N Normal(0, 1) draws made on the GPU by torch's
+    seeded generator (rank r: seed s * 1000 + 100 * tag + r) -- for buffers
+    too large to draw and copy from the host.  fp32 or bf16."""
+    import torch
+    out = []
+    for r in range(W):
+        g = torch.Generator(device=device)
+        g.manual_seed(seed * 1000 + 100 * tag + r)
+        x = torch.randn(N, generator=g, device=device, dtype=torch.float32)
+        out.append(x if dtype == "fp32" else x.to(torch.bfloat16))
+    return out
