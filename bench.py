@@ -405,66 +405,75 @@ class Step:
         if self.collective == "allreduce_rmsnorm":
             ins, res, wt = synth.workload_norm_operands(self.workload)
             self.host_in = ins + [res, wt]
-            self.xs = [dev_t(h) for h in ins]
-            self.res, self.wt = dev_t(res), dev_t(wt)
-            self.ys = [torch.empty_like(x) for x in self.xs] + [torch.empty_like(self.res)]
             H = w["hidden"]
             self.bytes = (2 * W + 2) * N * b + H * b
-            self.call = lambda: mr.mr_allreduce_rmsnorm(self.xs, self.ys[:W], self.wt, residual=self.res,
-                                                        residual_out=self.ys[W], eps=1e-6, algo=self.algo)
-            self.in_bytes = sum(x.numel() * b for x in self.xs) + self.res.numel() * b + H * b
-            self.out_bytes = sum(y.numel() * b for y in self.ys)
-            self.e2e_in = self.xs + [self.res, self.wt]
-            return
-        if self.collective.endswith("sign_ef"):
+            dins = [dev_t(h) for h in self.host_in]
+            douts = [torch.empty_like(x) for x in dins[:W]] + [torch.empty_like(dins[W])]
+
+            def bind(i, o):
+                return lambda: mr.mr_allreduce_rmsnorm(i[:W], o[:W], i[W + 1], residual=i[W], residual_out=o[W],
+                                                       eps=1e-6, algo=self.algo)
+        elif self.collective.endswith("sign_ef"):
             g, e = synth.workload_sign_operands(self.workload, N=N)
             self.host_in = g + e
-            self.xs = [dev_t(h) for h in g]
-            self.err = [dev_t(h) for h in e]
             rs = self.collective.startswith("reduce_scatter")
-            self.ys = [torch.empty(C if rs else N, dtype=tdt, device=dev) for _ in range(W)]
+            dins = [dev_t(h) for h in self.host_in]
+            douts = [torch.empty(C if rs else N, dtype=tdt, device=dev) for _ in range(W)] + dins[W:]
             self.scales = torch.empty(W, dtype=torch.float32, device=dev)
             self.ws = torch.empty(mr.mr_sign_ef_workspace_bytes(W, N), dtype=torch.uint8, device=dev)
             fn = mr.mr_reduce_scatter_sign_ef if rs else mr.mr_allreduce_sign_ef
             # two passes: read g, e for the norm; read them again, write e and the output
             self.bytes = 5 * W * N * b + (N if rs else W * N) * b
-            self.call = lambda: fn(self.xs, self.err, self.ys, scales=self.scales, workspace=self.ws, op=self.op,
-                                   algo=self.algo)
-            self.in_bytes = 2 * W * N * b
-            self.out_bytes = sum(y.numel() * b for y in self.ys) + W * N * b
-            self.e2e_in = self.xs + self.err
-            self.e2e_extra_out = self.err
             self.launches_per_step = 2
-            return
-        if self.collective == "all_gather":
+
+            def bind(i, o):
+                return lambda: fn(i[:W], i[W:], o[:W], scales=self.scales, workspace=self.ws, op=self.op,
+                                  algo=self.algo)
+        elif self.collective == "all_gather":
             self.host_in = synth.workload_param_shards(self.workload, N=N) if "param_dist" in w else \
                 [h[:C].copy() for h in synth.workload_inputs(self.workload, N=N)]
-            self.xs = [dev_t(h) for h in self.host_in]
-            self.ys = [torch.empty(N, dtype=tdt, device=dev) for _ in range(W)]
+            dins = [dev_t(h) for h in self.host_in]
+            douts = [torch.empty(N, dtype=tdt, device=dev) for _ in range(W)]
             self.bytes = (1 + W) * N * b
-            self.call = lambda: mr.mr_all_gather(self.xs, self.ys)
+
+            def bind(i, o):
+                return lambda: mr.mr_all_gather(i, o)
         else:
             self.host_in = synth.workload_inputs(self.workload, N=N)
-            self.xs = [dev_t(h) for h in self.host_in]
+            dins = [dev_t(h) for h in self.host_in]
             if self.collective == "allreduce":
-                self.ys = [torch.empty_like(x) for x in self.xs]
+                douts = [torch.empty_like(x) for x in dins]
                 self.bytes = 2 * W * N * b
-                if ex:
-                    self.call = lambda: mr.mr_allreduce_ex(self.xs, self.ys, op=self.op, algo=self.algo,
-                                                           group=self.group, per_hop=self.per_hop)
-                else:
-                    self.call = lambda: mr.mr_allreduce(self.xs, self.ys, op=self.op, algo=self.algo)
+
+                def bind(i, o):
+                    if ex:
+                        return lambda: mr.mr_allreduce_ex(i, o, op=self.op, algo=self.algo, group=self.group,
+                                                          per_hop=self.per_hop)
+                    return lambda: mr.mr_allreduce(i, o, op=self.op, algo=self.algo)
             else:
-                self.ys = [torch.empty(C, dtype=tdt, device=dev) for _ in range(W)]
+                douts = [torch.empty(C, dtype=tdt, device=dev) for _ in range(W)]
                 self.bytes = (W + 1) * N * b
-                if ex:
-                    self.call = lambda: mr.mr_reduce_scatter_ex(self.xs, self.ys, op=self.op, algo=self.algo,
-                                                                group=self.group, per_hop=self.per_hop)
-                else:
-                    self.call = lambda: mr.mr_reduce_scatter(self.xs, self.ys, op=self.op, algo=self.algo)
-        self.in_bytes = sum(x.numel() * b for x in self.xs)
-        self.out_bytes = sum(y.numel() * b for y in self.ys)
-        self.e2e_in = self.xs
+
+                def bind(i, o):
+                    if ex:
+                        return lambda: mr.mr_reduce_scatter_ex(i, o, op=self.op, algo=self.algo, group=self.group,
+                                                               per_hop=self.per_hop)
+                    return lambda: mr.mr_reduce_scatter(i, o, op=self.op, algo=self.algo)
+        self._bind = bind
+        self.e2e_in, self.e2e_out = dins, douts
+        self.xs, self.ys = dins[:W], douts[:W]
+        self.call = bind(dins, douts)
+        self.in_bytes = sum(x.numel() * x.element_size() for x in dins)
+        self.out_bytes = sum(y.numel() * y.element_size() for y in douts)
+
+    def make_set(self, torch):
+        """A second set of device buffers and the call bound to it (for
+        pipelining host copies of one step with the kernels of another).
+        Buffers that are both input and output stay shared within the set."""
+        fresh = {id(t): torch.empty_like(t) for t in self.e2e_in}
+        ins = [fresh[id(t)] for t in self.e2e_in]
+        outs = [fresh.get(id(t)) if id(t) in fresh else torch.empty_like(t) for t in self.e2e_out]
+        return ins, outs, self._bind(ins, outs)
 
     def config(self):
         kernel = {"allreduce": "fused all-reduce", "reduce_scatter": "reduce-scatter",
@@ -576,33 +585,60 @@ def run_mine(args):
                 "kernel": S.config()["kernel"], "algorithmic_bytes_per_launch": bytes_step,
                 "kernel_ms_mean": kern_ms}
 
-    # end to end through the public API: pinned host inputs in, results out
+    # End to end through the public API: every step copies its inputs in from
+    # pinned host memory, runs the call and copies its result out.  Steps are
+    # pipelined over two device buffer sets and three streams: the copy-in of
+    # step t+1 and the copy-out of step t-1 overlap the call of step t (the
+    # host link is full duplex); events keep each set's reuse in order.
     e2e = None
     if rank == 0 or world > 1:
         import numpy as np
         hin = [torch.from_numpy(np.ascontiguousarray(h).view(np.uint8)).pin_memory() for h in host]
-        outs_e2e = list(ys) + list(getattr(S, "e2e_extra_out", []))
-        hout = [torch.empty(y.numel() * y.element_size(), dtype=torch.uint8).pin_memory() for y in outs_e2e]
+        hout = [torch.empty(y.numel() * y.element_size(), dtype=torch.uint8).pin_memory() for y in S.e2e_out]
+        sets = [(S.e2e_in, S.e2e_out, S.call), S.make_set(torch)]
+        s_in, s_cmp, s_out = torch.cuda.Stream(), torch.cuda.Stream(), torch.cuda.Stream()
+        done_k = [None, None]     # the call of the last step on each set (inputs free)
+        done_o = [None, None]     # the copy-out of the last step on each set (outputs free)
 
-        def e2e_step():
-            for x, h in zip(S.e2e_in, hin):
-                x.view(torch.uint8).copy_(h, non_blocking=True)
-            step()
-            for h, y in zip(hout, outs_e2e):
-                h.copy_(y.view(torch.uint8), non_blocking=True)
-        e2e_step()
+        def e2e_step(t):
+            ins, outs, call = sets[t % 2]
+            with torch.cuda.stream(s_in):
+                if done_k[t % 2] is not None:
+                    s_in.wait_event(done_k[t % 2])
+                for x, h in zip(ins, hin):
+                    x.view(torch.uint8).copy_(h, non_blocking=True)
+                e_in = torch.cuda.Event()
+                e_in.record(s_in)
+            with torch.cuda.stream(s_cmp):
+                s_cmp.wait_event(e_in)
+                if done_o[t % 2] is not None:
+                    s_cmp.wait_event(done_o[t % 2])
+                call()
+                e_k = torch.cuda.Event()
+                e_k.record(s_cmp)
+                done_k[t % 2] = e_k
+            with torch.cuda.stream(s_out):
+                s_out.wait_event(e_k)
+                for h, y in zip(hout, outs):
+                    h.copy_(y.view(torch.uint8), non_blocking=True)
+                e_o = torch.cuda.Event()
+                e_o.record(s_out)
+                done_o[t % 2] = e_o
+
+        for t in range(2):
+            e2e_step(t)
         torch.cuda.synchronize()
         a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        a.record()
-        for _ in range(args.e2e_steps):
-            e2e_step()
-        b.record()
+        a.record(s_in)
+        for t in range(args.e2e_steps):
+            e2e_step(t)
+        b.record(s_out)
         torch.cuda.synchronize()
         e_ms = a.elapsed_time(b) / args.e2e_steps
         e2e = {"value": bytes_step / (e_ms * 1e-3) / 1e9, "unit": "GB/s", "ms_per_step": e_ms,
                "h2d_bytes_per_step": S.in_bytes, "d2h_bytes_per_step": S.out_bytes,
-               "steps": args.e2e_steps}
-        del hin, hout
+               "steps": args.e2e_steps, "pipelined": "2 buffer sets, copy-in / call / copy-out streams"}
+        del hin, hout, sets
 
     extra = None
     if rank == 0 and world == 1 and not args.no_extras and headline:
