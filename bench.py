@@ -246,24 +246,101 @@ def workload_config(W, N):
 # the CUDA path
 # ---------------------------------------------------------------------------
 
-def time_calls(fn, iters, flush=None):
-    """Median, mean, min and max device time (ms) of fn over iters calls, each
-    bracketed by its own events on the current stream; flush() runs outside
-    the events.  The stream is first held by a device-side sleep while the
-    host enqueues every call, so small calls are timed on the device rather
-    than at the host's launch rate."""
+def back_to_back_us(fn, n=100, reps=5):
+    """Device time per call (us) of n calls queued back to back on the current
+    stream, with one event pair around all n (the nccl-tests way): the launches
+    overlap as they would in a training loop.  The stream is first held by a
+    device-side sleep while the host enqueues, so small calls are timed on the
+    device rather than at the host's launch rate.  Best of reps."""
     import torch
-    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(iters)]
-    torch.cuda._sleep(20_000_000)
-    for a, b in evs:
-        if flush is not None:
-            flush()
+    best = float("inf")
+    for _ in range(reps):
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize()
+        torch.cuda._sleep(20_000_000)
         a.record()
-        fn()
+        for _ in range(n):
+            fn()
         b.record()
+        torch.cuda.synchronize()
+        best = min(best, a.elapsed_time(b) * 1e3 / n)
+    return best
+
+
+def capture(fn, n):
+    """A CUDA graph of n consecutive calls of fn."""
+    import torch
+    g = torch.cuda.CUDAGraph()
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        fn()
+        with torch.cuda.graph(g, stream=side):
+            for _ in range(n):
+                fn()
+    torch.cuda.current_stream().wait_stream(side)
     torch.cuda.synchronize()
-    ts = [a.elapsed_time(b) for a, b in evs]
-    return statistics.median(ts), statistics.mean(ts), min(ts), max(ts)
+    return g
+
+
+def graph_us(fn, n=50, reps=5):
+    """Device time per call (us) of a CUDA graph of n calls, best of reps replays."""
+    import torch
+    g = capture(fn, n)
+    g.replay()
+    best = float("inf")
+    for _ in range(reps):
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize()
+        a.record()
+        g.replay()
+        b.record()
+        torch.cuda.synchronize()
+        best = min(best, a.elapsed_time(b) * 1e3 / n)
+    del g
+    return best
+
+
+def cold_l2_us(fn, flush, n=20):
+    """Device time per call (us) with L2 flushed before every call: a graph of n
+    (flush, call) pairs minus a graph of n flushes."""
+    def both():
+        flush()
+        fn()
+    return max(0.0, graph_us(both, n) - graph_us(flush, n))
+
+
+def carve(torch, dev, specs):
+    """Device buffers for (numel, torch dtype) specs, cut in order out of ONE
+    allocation, each starting on a 256-byte boundary.  The rank buffers of a
+    step live side by side in HBM, the way a framework's flat buffers do;
+    measured on GB300 this ran the W=8 all-reduce at 6633 GB/s against 6392
+    GB/s for 16 separate allocations of the same buffers."""
+    offs, total = [], 0
+    for n, dt in specs:
+        total = (total + 255) // 256 * 256
+        offs.append(total)
+        total += n * torch.empty((), dtype=dt).element_size()
+    slab = torch.empty(max(total, 1), dtype=torch.uint8, device=dev)
+    out = []
+    for (n, dt), o in zip(specs, offs):
+        es = torch.empty((), dtype=dt).element_size()
+        out.append(slab[o:o + n * es].view(dt))
+    return out
+
+
+def upload(torch, dev, hosts, dtype, extra=()):
+    """Device copies of raw host rank buffers (fp32 / bf16 bits / int32), then
+    fresh buffers of the `extra` lengths, all carved from one allocation."""
+    import numpy as np
+    tdt = {"fp32": torch.float32, "bf16": torch.bfloat16, "int32": torch.int32}[dtype]
+    bufs = carve(torch, dev, [(h.size, tdt) for h in hosts] + [(n, tdt) for n in extra])
+    for b, h in zip(bufs, hosts):
+        if dtype == "bf16":
+            b.view(torch.int16).copy_(torch.from_numpy(np.ascontiguousarray(h).view(np.int16)))
+        else:
+            b.copy_(torch.from_numpy(np.ascontiguousarray(h)))
+    return bufs[:len(hosts)], bufs[len(hosts):]
 
 
 def host_call_us(fn, iters=300):
@@ -295,67 +372,73 @@ def extras(mr, torch, dev):
     W = 8
     for N in synth.WORKLOADS["sweep_fp32_w8"]["Ns"]:
         host = synth.workload_inputs("sweep_fp32_w8", N=N)
-        xs = [torch.from_numpy(h).to(dev) for h in host]
-        ys = [torch.empty_like(x) for x in xs]
-        row = {"N_per_rank": N, "bytes_per_rank": N * 4}
+        xs, ys = upload(torch, dev, host, "fp32", [N] * W)
+        by = 2 * W * N * 4
+        row = {"N_per_rank": N, "bytes_per_rank": N * 4, "bytes_per_call": by}
         row["auto_picks"] = mr.mr_plan_auto(W, N, "fp32")[0]
+        n = 200 if by <= (64 << 20) else 20
         for algo in ("ring", "tree", "auto"):
             def call():
                 mr.mr_allreduce(xs, ys, op="sum", algo=algo)
             for _ in range(5):
                 call()
-            med, _, _, _ = time_calls(call, 30)
-            row[f"{algo}_us"] = med * 1e3
-            row[f"{algo}_gbs"] = 2 * W * N * 4 / (med * 1e-3) / 1e9
-            if 2 * W * N * 4 < 4 * L2_BYTES:
-                fmed, _, _, _ = time_calls(call, 30, flush)
-                row[f"{algo}_flushed_us"] = fmed * 1e3
-                row[f"{algo}_flushed_gbs"] = 2 * W * N * 4 / (fmed * 1e-3) / 1e9
+            t = back_to_back_us(call, n)
+            row[f"{algo}_us"] = t
+            row[f"{algo}_gbs"] = by / (t * 1e-6) / 1e9
+            if by < GRAPH_BELOW_BYTES:
+                t = graph_us(call, 50)
+                row[f"{algo}_graph_us"] = t
+                row[f"{algo}_graph_gbs"] = by / (t * 1e-6) / 1e9
+            if by < 4 * L2_BYTES:
+                t = cold_l2_us(call, flush)
+                row[f"{algo}_cold_l2_us"] = t
+                row[f"{algo}_cold_l2_gbs"] = by / (t * 1e-6) / 1e9 if t > 0 else None
         if N == (1 << 10):
             row["host_call_us"] = host_call_us(lambda: mr.mr_allreduce(xs, ys, op="sum", algo="ring"))
         sweep.append(row)
         del xs, ys
-    out["sweep_fp32_w8_sum"] = sweep
+    out["sweep_fp32_w8_sum"] = {
+        "timing": ("us per call: back to back on one stream, one event pair around 200 calls (20 above 64 MiB); "
+                   "graph: a CUDA graph of 50 calls; cold_l2: L2 flushed before every call (graph of flush+call "
+                   "minus graph of flushes); working sets below 4x L2 are otherwise warm"),
+        "rows": sweep}
 
     # FSDP: reduce-scatter avg of bf16 gradients, all-gather of bf16 parameter shards
     host = synth.workload_inputs("fsdp_bf16_w8")
     W, N = len(host), host[0].size
-    xs = [torch.from_numpy(h.view(np.int16)).to(dev).view(torch.bfloat16) for h in host]
-    shards = [torch.empty(N // W, dtype=torch.bfloat16, device=dev) for _ in range(W)]
-    full = [torch.empty(N, dtype=torch.bfloat16, device=dev) for _ in range(W)]
+    xs, bufs = upload(torch, dev, host, "bf16", [N // W] * W + [N] * W)
+    shards, full = bufs[:W], bufs[W:]
     rs = lambda: mr.mr_reduce_scatter(xs, shards, op="avg", algo="ring")  # noqa: E731
     ag = lambda: mr.mr_all_gather(shards, full)  # noqa: E731
     for _ in range(3):
         rs()
         ag()
-    rmed, _, _, _ = time_calls(rs, 20)
-    amed, _, _, _ = time_calls(ag, 20)
+    rt = back_to_back_us(rs, 20)
+    at = back_to_back_us(ag, 20)
     out["fsdp_bf16_w8"] = {
-        "reduce_scatter_us": rmed * 1e3, "reduce_scatter_gbs": (W + 1) * N * 2 / (rmed * 1e-3) / 1e9,
-        "all_gather_us": amed * 1e3, "all_gather_gbs": (W + 1) * N * 2 / (amed * 1e-3) / 1e9}
+        "reduce_scatter_us": rt, "reduce_scatter_gbs": (W + 1) * N * 2 / (rt * 1e-6) / 1e9,
+        "all_gather_us": at, "all_gather_gbs": (W + 1) * N * 2 / (at * 1e-6) / 1e9}
     del xs, shards, full
 
     # integer counts: W=16 int32
     host = synth.workload_inputs("int_counts_w16")
     W, N = len(host), host[0].size
-    xs = [torch.from_numpy(h).to(dev) for h in host]
-    ys = [torch.empty_like(x) for x in xs]
+    xs, ys = upload(torch, dev, host, "int32", [N] * W)
     row = {}
     for op in ("sum", "max"):
         for algo in ("ring", "tree"):
             f = lambda: mr.mr_allreduce(xs, ys, op=op, algo=algo)  # noqa: E731
             f()
-            med, _, _, _ = time_calls(f, 20)
-            row[f"{op}_{algo}_gbs"] = 2 * W * N * 4 / (med * 1e-3) / 1e9
+            t = back_to_back_us(f, 20)
+            row[f"{op}_{algo}_gbs"] = 2 * W * N * 4 / (t * 1e-6) / 1e9
     out["int_counts_w16"] = row
     del xs, ys
 
     # fused all-reduce against reduce-scatter followed by all-gather (DDP bucket)
     host = synth.workload_inputs(WORKLOAD)
     W, N = len(host), host[0].size
-    xs = [torch.from_numpy(h).to(dev) for h in host]
-    ys = [torch.empty_like(x) for x in xs]
-    sh = [torch.empty(N // W, device=dev) for _ in range(W)]
+    xs, bufs = upload(torch, dev, host, "fp32", [N] * W + [N // W] * W)
+    ys, sh = bufs[:W], bufs[W:]
     fused = lambda: mr.mr_allreduce(xs, ys, op="avg", algo="ring")  # noqa: E731
 
     def unfused():
@@ -363,9 +446,9 @@ def extras(mr, torch, dev):
         mr.mr_all_gather(sh, ys)
     fused()
     unfused()
-    fmed, _, _, _ = time_calls(fused, 20)
-    umed, _, _, _ = time_calls(unfused, 20)
-    out["fused_vs_unfused_ddp_bucket"] = {"fused_us": fmed * 1e3, "rs_then_ag_us": umed * 1e3,
+    ft = back_to_back_us(fused, 20)
+    ut = back_to_back_us(unfused, 20)
+    out["fused_vs_unfused_ddp_bucket"] = {"fused_us": ft, "rs_then_ag_us": ut,
                                           "fused_bytes": 2 * W * N * 4, "unfused_bytes": (2 * W + 2) * N * 4}
     return out
 
@@ -380,8 +463,8 @@ class Step:
                 "sign_ef_fp32_w8": ("reduce_scatter_sign_ef", "avg"), "hier_bf16_w16": ("allreduce", "avg")}
 
     def __init__(self, args, mr, torch, dev):
-        import numpy as np
         import synth
+        self.dev = dev
         self.launches_per_step = 1
         self.workload = args.workload
         w = synth.WORKLOADS[self.workload]
@@ -399,16 +482,12 @@ class Step:
         b = 2 if self.dtype == "bf16" else 4
         C = N // W
 
-        def dev_t(h):
-            return torch.from_numpy(h.view(np.int16) if self.dtype == "bf16" else h).to(dev).view(tdt)
-
         if self.collective == "allreduce_rmsnorm":
             ins, res, wt = synth.workload_norm_operands(self.workload)
             self.host_in = ins + [res, wt]
             H = w["hidden"]
             self.bytes = (2 * W + 2) * N * b + H * b
-            dins = [dev_t(h) for h in self.host_in]
-            douts = [torch.empty_like(x) for x in dins[:W]] + [torch.empty_like(dins[W])]
+            dins, douts = upload(torch, dev, self.host_in, self.dtype, [N] * (W + 1))
 
             def bind(i, o):
                 return lambda: mr.mr_allreduce_rmsnorm(i[:W], o[:W], i[W + 1], residual=i[W], residual_out=o[W],
@@ -417,8 +496,8 @@ class Step:
             g, e = synth.workload_sign_operands(self.workload, N=N)
             self.host_in = g + e
             rs = self.collective.startswith("reduce_scatter")
-            dins = [dev_t(h) for h in self.host_in]
-            douts = [torch.empty(C if rs else N, dtype=tdt, device=dev) for _ in range(W)] + dins[W:]
+            dins, douts = upload(torch, dev, self.host_in, self.dtype, [C if rs else N] * W)
+            douts = douts + dins[W:]
             self.scales = torch.empty(W, dtype=torch.float32, device=dev)
             self.ws = torch.empty(mr.mr_sign_ef_workspace_bytes(W, N), dtype=torch.uint8, device=dev)
             fn = mr.mr_reduce_scatter_sign_ef if rs else mr.mr_allreduce_sign_ef
@@ -432,17 +511,15 @@ class Step:
         elif self.collective == "all_gather":
             self.host_in = synth.workload_param_shards(self.workload, N=N) if "param_dist" in w else \
                 [h[:C].copy() for h in synth.workload_inputs(self.workload, N=N)]
-            dins = [dev_t(h) for h in self.host_in]
-            douts = [torch.empty(N, dtype=tdt, device=dev) for _ in range(W)]
+            dins, douts = upload(torch, dev, self.host_in, self.dtype, [N] * W)
             self.bytes = (1 + W) * N * b
 
             def bind(i, o):
                 return lambda: mr.mr_all_gather(i, o)
         else:
             self.host_in = synth.workload_inputs(self.workload, N=N)
-            dins = [dev_t(h) for h in self.host_in]
+            dins, douts = upload(torch, dev, self.host_in, self.dtype, [N if self.collective == "allreduce" else C] * W)
             if self.collective == "allreduce":
-                douts = [torch.empty_like(x) for x in dins]
                 self.bytes = 2 * W * N * b
 
                 def bind(i, o):
@@ -451,7 +528,6 @@ class Step:
                                                           per_hop=self.per_hop)
                     return lambda: mr.mr_allreduce(i, o, op=self.op, algo=self.algo)
             else:
-                douts = [torch.empty(C, dtype=tdt, device=dev) for _ in range(W)]
                 self.bytes = (W + 1) * N * b
 
                 def bind(i, o):
@@ -470,9 +546,11 @@ class Step:
         """A second set of device buffers and the call bound to it (for
         pipelining host copies of one step with the kernels of another).
         Buffers that are both input and output stay shared within the set."""
-        fresh = {id(t): torch.empty_like(t) for t in self.e2e_in}
+        own = [t for t in self.e2e_out if all(t is not x for x in self.e2e_in)]
+        bufs = carve(torch, self.dev, [(t.numel(), t.dtype) for t in self.e2e_in + own])
+        fresh = {id(t): f for t, f in zip(self.e2e_in + own, bufs)}
         ins = [fresh[id(t)] for t in self.e2e_in]
-        outs = [fresh.get(id(t)) if id(t) in fresh else torch.empty_like(t) for t in self.e2e_out]
+        outs = [fresh[id(t)] for t in self.e2e_out]
         return ins, outs, self._bind(ins, outs)
 
     def config(self):
@@ -524,21 +602,12 @@ def run_mine(args):
         dist.barrier()
 
     # Small steps are launch-bound from Python: time them as replays of a CUDA
-    # graph holding kGraph consecutive steps, so the events see device time.
+    # graph holding GRAPH_STEPS consecutive steps, so the events see device time.
     use_graph = S.bytes < GRAPH_BELOW_BYTES
     timed_step = step
     per_replay = 1
     if use_graph:
-        g = torch.cuda.CUDAGraph()
-        side = torch.cuda.Stream()
-        side.wait_stream(torch.cuda.current_stream())
-        with torch.cuda.stream(side):
-            step()
-        torch.cuda.current_stream().wait_stream(side)
-        with torch.cuda.graph(g):
-            for _ in range(GRAPH_STEPS):
-                step()
-        torch.cuda.synchronize()
+        g = capture(step, GRAPH_STEPS)
         timed_step = g.replay
         per_replay = GRAPH_STEPS
         for _ in range(3):
@@ -552,8 +621,9 @@ def run_mine(args):
     sampler = ClockSampler(gpu_index)
     sampler.start()
     K = max(per_replay, (args.steps // per_replay) * per_replay)
-    per = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-           for _ in range(K // per_replay)]
+    # The timed region: K steps queued back to back, one event pair around them
+    # all.  An event between steps would stand between two launches and keep
+    # the next launch from overlapping the tail of the one before.
     t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     torch.cuda.synchronize()
     if dist:
@@ -561,10 +631,8 @@ def run_mine(args):
     launches0 = mr.mr_launch_count()
     sampler.mark(True)
     t_start.record()
-    for a, b in per:
-        a.record()
+    for _ in range(K // per_replay):
         timed_step()
-        b.record()
     t_end.record()
     torch.cuda.synchronize()
     sampler.mark(False)
@@ -573,17 +641,31 @@ def run_mine(args):
     # a graph replay launches its captured kernels without calling the library
     launches = (mr.mr_launch_count() - launches0) if not use_graph else K * S.launches_per_step
     clocks = sampler.stop()
-    total_ms = t_start.elapsed_time(t_end)
-    kern_ms = statistics.mean(a.elapsed_time(b) for a, b in per) / per_replay
-    total_ms = slowest_rank_ms(total_ms, dist, dev)
+    local_ms = t_start.elapsed_time(t_end)
+    total_ms = slowest_rank_ms(local_ms, dist, dev)
     value = job_gbs(world, bytes_step, K, total_ms)
+
+    # The dominant kernel's average launch duration over the timed region: the
+    # region holds nothing but this step's launches, back to back.
+    kern_ms = local_ms / K
+    # For comparison, one launch at a time: an event pair around each (this
+    # includes the launch gap that back-to-back launches hide).
+    iso = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(20)]
+    for e0, e1 in iso:
+        e0.record()
+        step()
+        e1.record()
+    torch.cuda.synchronize()
+    iso_ms = statistics.median(e0.elapsed_time(e1) for e0, e1 in iso)
 
     peak, peak_src = peaks()
     achieved = bytes_step / (kern_ms * 1e-3) / 1e9
     roofline = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
                 "traffic": profiled_traffic() if headline else None, "peak_source": peak_src,
                 "kernel": S.config()["kernel"], "algorithmic_bytes_per_launch": bytes_step,
-                "kernel_ms_mean": kern_ms}
+                "kernel_ms_mean": kern_ms, "launches_per_step": S.launches_per_step,
+                "duration": "timed region / steps (steps back to back on one stream)",
+                "step_ms_one_at_a_time": iso_ms}
 
     # End to end through the public API: every step copies its inputs in from
     # pinned host memory, runs the call and copies its result out.  Steps are
@@ -591,7 +673,7 @@ def run_mine(args):
     # step t+1 and the copy-out of step t-1 overlap the call of step t (the
     # host link is full duplex); events keep each set's reuse in order.
     e2e = None
-    if rank == 0 or world > 1:
+    if args.e2e_steps > 0 and (rank == 0 or world > 1):
         import numpy as np
         hin = [torch.from_numpy(np.ascontiguousarray(h).view(np.uint8)).pin_memory() for h in host]
         hout = [torch.empty(y.numel() * y.element_size(), dtype=torch.uint8).pin_memory() for y in S.e2e_out]

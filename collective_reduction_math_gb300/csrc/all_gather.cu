@@ -17,6 +17,7 @@ namespace mr {
 
 __global__ void __launch_bounds__(kThreads)
 all_gather_kernel(const __grid_constant__ GatherParams P) {
+    pdl_enter();
     const int W = P.W;
     const uint64_t shard_bytes = P.C * (uint64_t)P.esize;
 
@@ -70,8 +71,7 @@ all_gather_kernel(const __grid_constant__ GatherParams P) {
 }
 
 cudaError_t launch_all_gather(const GatherParams& P, dim3 grid, cudaStream_t s) {
-    all_gather_kernel<<<grid, kThreads, 0, s>>>(P);
-    return cudaGetLastError();
+    return launch_kernel(all_gather_kernel, grid, 0, s, 0, P);
 }
 
 }  // namespace mr

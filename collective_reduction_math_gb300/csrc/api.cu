@@ -323,6 +323,14 @@ mr_status_t run_reduce(const char* what, int mode, const void* const* send, void
 }  // namespace
 
 namespace mr {
+bool pdl_enabled() {
+    static const bool on = [] {
+        const char* e = getenv("MR_PDL");
+        return !(e && e[0] == '0');
+    }();
+    return on;
+}
+
 // Records `fmt` as the calling thread's last error and returns `st` (for
 // entry points defined in other translation units).
 mr_status_t report_error(mr_status_t st, const char* fmt, ...) {

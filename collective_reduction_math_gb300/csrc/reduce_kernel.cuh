@@ -43,16 +43,25 @@ template <> struct Elem<MR_BF16> { using raw_t = uint16_t; using acc_t = float; 
 template <> struct Elem<MR_INT32> { using raw_t = uint32_t; using acc_t = uint32_t; static constexpr int kBytes = 4; };
 
 // Total-order key of an fp32 value: a signed integer that orders -0 below +0
-// and otherwise follows the numeric order (NaN excluded).
+// and otherwise follows the numeric order (NaN excluded).  The map flips the
+// magnitude bits of negative values and is its own inverse.
 __device__ __forceinline__ int32_t f32_order_key(float x) {
     int32_t b = __float_as_int(x);
     return b ^ ((b >> 31) & 0x7FFFFFFF);
+}
+__device__ __forceinline__ float f32_from_order_key(int32_t k) {
+    return __int_as_float(k ^ ((k >> 31) & 0x7FFFFFFF));
 }
 
 template <int DT, int OP> struct Arith {
     using E = Elem<DT>;
     using raw_t = typename E::raw_t;
     using acc_t = typename E::acc_t;
+    // Float min and max run in the order-key domain: each contribution is
+    // mapped to its key once as it is read, the fold is an integer min / max
+    // (one instruction per combine), and post maps the result back.  The map
+    // is a bijection that preserves the order, so this is exact.
+    static constexpr bool kKeyed = DT != MR_INT32 && (OP == MR_MIN || OP == MR_MAX);
 
     // Read one contribution: widen, and pre-scale a float avg by fl32(1/W).
     static __device__ __forceinline__ acc_t read(raw_t x, float s) {
@@ -61,6 +70,7 @@ template <int DT, int OP> struct Arith {
         } else {
             float f = (DT == MR_FP32) ? __uint_as_float(x) : __uint_as_float((uint32_t)x << 16);
             if constexpr (OP == MR_AVG) f = __fmul_rn(f, s);
+            if constexpr (kKeyed) return __int_as_float(f32_order_key(f));
             return f;
         }
     }
@@ -69,25 +79,27 @@ template <int DT, int OP> struct Arith {
         if constexpr (DT == MR_INT32) {
             if constexpr (OP == MR_SUM || OP == MR_AVG) return a + b;   // wraps mod 2^32
             if constexpr (OP == MR_PROD) return a * b;
-            if constexpr (OP == MR_MIN) return ((int32_t)b < (int32_t)a) ? b : a;
-            if constexpr (OP == MR_MAX) return ((int32_t)a < (int32_t)b) ? b : a;
+            if constexpr (OP == MR_MIN) return (uint32_t)::min((int32_t)a, (int32_t)b);
+            if constexpr (OP == MR_MAX) return (uint32_t)::max((int32_t)a, (int32_t)b);
         } else {
             if constexpr (OP == MR_SUM || OP == MR_AVG) return __fadd_rn(a, b);
             if constexpr (OP == MR_PROD) return __fmul_rn(a, b);
-            if constexpr (OP == MR_MIN) return (f32_order_key(b) < f32_order_key(a)) ? b : a;
-            if constexpr (OP == MR_MAX) return (f32_order_key(a) < f32_order_key(b)) ? b : a;
+            if constexpr (OP == MR_MIN) return __int_as_float(::min(__float_as_int(a), __float_as_int(b)));
+            if constexpr (OP == MR_MAX) return __int_as_float(::max(__float_as_int(a), __float_as_int(b)));
         }
     }
 
     // Per-hop rounding: a bf16 running total rounded to bf16 (as it would
-    // cross a wire); the identity for fp32 and int32.
+    // cross a wire); the identity for fp32 and int32, and for min and max,
+    // whose running value is always one of the bf16 contributions.
     static __device__ __forceinline__ acc_t hop(acc_t a) {
-        if constexpr (DT == MR_BF16) return __uint_as_float((uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(a)) << 16);
+        if constexpr (DT == MR_BF16 && !kKeyed) return __uint_as_float((uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(a)) << 16);
         else return a;
     }
 
     // The postOp where the sum completes.
     static __device__ __forceinline__ raw_t post(acc_t a, int W) {
+        if constexpr (kKeyed) a = f32_from_order_key(__float_as_int(a));
         if constexpr (DT == MR_FP32) return __float_as_uint(a);
         if constexpr (DT == MR_BF16) return __bfloat16_as_ushort(__float2bfloat16_rn(a));
         if constexpr (DT == MR_INT32) {
@@ -232,18 +244,20 @@ template <class raw_t, int VB> __device__ __forceinline__ void set_lane(Vec<VB>&
 }
 
 // The vector path's fold: all LANES elements of one vector at once.  The
-// hierarchical order, and the ring on 8-lane (bf16) vectors, run positions
-// outer and lanes inner, so each position's (warp-uniform) decisions --
-// inside W, start of a group, per-hop rounding -- are taken once per vector
-// rather than once per lane; the tree, and the ring on 4-lane vectors, run
-// lane by lane (measured faster for fp32 on GB300).  contrib(x) widens,
-// pre-scales and (per-hop) rounds one raw contribution.
+// hierarchical order, and the ring on bf16 (8-lane) and int32 vectors, run
+// positions outer and lanes inner, so each position's (warp-uniform)
+// decisions -- inside W, start of a group, per-hop rounding -- are taken once
+// per vector rather than once per lane; the tree, and the ring on fp32
+// vectors, run lane by lane.  Both choices were measured on GB300 (fp32 ring
+// sum faster lane by lane; int32 ring max at W = 16 6.0 against 4.8 TB/s
+// lanes inner).  contrib(x) widens, pre-scales and (per-hop) rounds one raw
+// contribution.
 template <class A, int ALGO, int WCAP, int VB, int LANES, class Contrib>
 __device__ __forceinline__ void fold_lanes(const Vec<VB> (&raw)[WCAP], int W, uint64_t gmask, bool hop,
                                            Contrib contrib, typename A::acc_t (&out)[LANES]) {
     using acc_t = typename A::acc_t;
     using raw_t = typename A::raw_t;
-    if constexpr (ALGO == MR_TREE || (ALGO == MR_RING && LANES <= 4)) {
+    if constexpr (ALGO == MR_TREE || (ALGO == MR_RING && LANES <= 4 && std::is_same<acc_t, float>::value)) {
 #pragma unroll
         for (int l = 0; l < LANES; ++l) {
             acc_t y[WCAP];
@@ -315,6 +329,8 @@ reduce_kernel(const __grid_constant__ ReduceParams P) {
     using acc_t = typename A::acc_t;
     constexpr int EB = Elem<DT>::kBytes;
     constexpr int LANES = VB / EB;
+
+    pdl_enter();    // the previous kernel on the stream has finished with our buffers
 
     const int W = P.W;
     const float s = P.scale;
@@ -505,19 +521,16 @@ cudaError_t launch_reduce(const ReduceParams& P, int op, dim3 grid, cudaStream_t
         constexpr int OP = decltype(op_c)::value;
         const bool rs = P.mode == MODE_REDUCE_SCATTER;
         switch (reduce_wcap(P.W)) {
-            case 2: reduce_kernel<DT, OP, ALGO, 2, 16, reduce_unroll_for(2, false), HOP><<<grid, kThreads, 0, stream>>>(P); break;
-            case 4: reduce_kernel<DT, OP, ALGO, 4, 16, reduce_unroll_for(4, false), HOP><<<grid, kThreads, 0, stream>>>(P); break;
+            case 2: return launch_kernel(reduce_kernel<DT, OP, ALGO, 2, 16, reduce_unroll_for(2, false), HOP>, grid, 0, stream, 0, P);
+            case 4: return launch_kernel(reduce_kernel<DT, OP, ALGO, 4, 16, reduce_unroll_for(4, false), HOP>, grid, 0, stream, 0, P);
             case 8:
-                if (rs) reduce_kernel<DT, OP, ALGO, 8, 16, reduce_unroll_for(8, true), HOP><<<grid, kThreads, 0, stream>>>(P);
-                else reduce_kernel<DT, OP, ALGO, 8, 16, reduce_unroll_for(8, false), HOP><<<grid, kThreads, 0, stream>>>(P);
-                break;
-            case 16: reduce_kernel<DT, OP, ALGO, 16, 16, reduce_unroll_for(16, false), HOP><<<grid, kThreads, 0, stream>>>(P); break;
+                if (rs) return launch_kernel(reduce_kernel<DT, OP, ALGO, 8, 16, reduce_unroll_for(8, true), HOP>, grid, 0, stream, 0, P);
+                return launch_kernel(reduce_kernel<DT, OP, ALGO, 8, 16, reduce_unroll_for(8, false), HOP>, grid, 0, stream, 0, P);
+            case 16: return launch_kernel(reduce_kernel<DT, OP, ALGO, 16, 16, reduce_unroll_for(16, false), HOP>, grid, 0, stream, 0, P);
             default:
-                reduce_kernel<DT, OP, ALGO, 64, reduce_vector_bytes(64, ALGO), reduce_unroll_for(64, false), HOP>
-                    <<<grid, kThreads, 0, stream>>>(P);
-                break;
+                return launch_kernel(reduce_kernel<DT, OP, ALGO, 64, reduce_vector_bytes(64, ALGO), reduce_unroll_for(64, false), HOP>,
+                                     grid, 0, stream, 0, P);
         }
-        return cudaGetLastError();
     };
     switch (op) {
         case MR_SUM: return go(std::integral_constant<int, MR_SUM>{});

@@ -35,6 +35,7 @@ namespace mr {
 template <int DT, int ALGO, int WCAP, int VB>
 __global__ void __launch_bounds__(kThreads, WCAP <= 8 ? 3 : WCAP <= 16 ? 2 : 1)
 allreduce_rmsnorm_kernel(const __grid_constant__ NormParams P) {
+    pdl_enter();
     using A = Arith<DT, MR_SUM>;
     using raw_t = typename A::raw_t;
     constexpr int EB = Elem<DT>::kBytes;
@@ -221,19 +222,7 @@ static cudaError_t launch_one(const NormParams& P, dim3 grid, size_t smem, cudaS
         const cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
         if (e != cudaSuccess) return e;
     }
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = grid;
-    cfg.blockDim = dim3(kThreads, 1, 1);
-    cfg.dynamicSmemBytes = smem;
-    cfg.stream = s;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = (unsigned)P.csize;
-    attr[0].val.clusterDim.y = 1;
-    attr[0].val.clusterDim.z = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, k, P);
+    return launch_kernel(k, grid, smem, s, (unsigned)P.csize, P);
 }
 
 template <int DT, int ALGO>

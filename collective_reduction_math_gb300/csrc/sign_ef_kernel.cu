@@ -53,6 +53,7 @@ __device__ __forceinline__ double block_sum_f64(double v, double* warp_part) {
 
 __global__ void __launch_bounds__(kThreads)
 sign_l1_kernel(const __grid_constant__ SignParams P) {
+    pdl_enter();
     __shared__ double warp_part[kThreads / 32];
     const int r = blockIdx.y, b = blockIdx.x;
     const float* g = static_cast<const float*>(P.grad[r]);
@@ -83,6 +84,7 @@ sign_ef_kernel(const __grid_constant__ SignParams P) {
     using A = Arith<MR_FP32, OP>;
     constexpr int LANES = VB / 4;
     __shared__ float scale[WCAP];
+    pdl_enter();    // also orders this kernel after the partials of sign_l1_kernel
 
     const int W = P.W;
     const bool rs = (P.mode == MODE_REDUCE_SCATTER);
@@ -194,16 +196,14 @@ sign_ef_kernel(const __grid_constant__ SignParams P) {
 }
 
 cudaError_t launch_sign_l1(const SignParams& P, cudaStream_t s) {
-    sign_l1_kernel<<<dim3((unsigned)P.nb, (unsigned)P.W, 1), kThreads, 0, s>>>(P);
-    return cudaGetLastError();
+    return launch_kernel(sign_l1_kernel, dim3((unsigned)P.nb, (unsigned)P.W, 1), 0, s, 0, P);
 }
 
 template <int OP, int ALGO>
 static cudaError_t launch_ef_algo(const SignParams& P, dim3 grid, cudaStream_t s) {
-    if (P.W <= 8) sign_ef_kernel<OP, ALGO, 8, 16><<<grid, kThreads, 0, s>>>(P);
-    else if (P.W <= 16) sign_ef_kernel<OP, ALGO, 16, 8><<<grid, kThreads, 0, s>>>(P);
-    else sign_ef_kernel<OP, ALGO, 64, 4><<<grid, kThreads, 0, s>>>(P);
-    return cudaGetLastError();
+    if (P.W <= 8) return launch_kernel(sign_ef_kernel<OP, ALGO, 8, 16>, grid, 0, s, 0, P);
+    if (P.W <= 16) return launch_kernel(sign_ef_kernel<OP, ALGO, 16, 8>, grid, 0, s, 0, P);
+    return launch_kernel(sign_ef_kernel<OP, ALGO, 64, 4>, grid, 0, s, 0, P);
 }
 
 cudaError_t launch_sign_ef(const SignParams& P, int op, int algo, dim3 grid, cudaStream_t s) {
