@@ -48,6 +48,12 @@
  *     stream) and is asynchronous: the call never synchronises, allocates no
  *     device memory and creates no streams.  Execution errors surface at the
  *     caller's next synchronisation.  N == 0 launches nothing and returns MR_OK.
+ *   - Kernels are launched with programmatic dependent launch: a launch may
+ *     begin while the kernel before it on the stream is finishing, and waits
+ *     for that kernel to complete before it reads or writes any buffer, so
+ *     stream order holds exactly as for a plain launch (also under CUDA graph
+ *     capture).  Setting MR_PDL=0 in the environment before the first call
+ *     launches every kernel in plain stream order instead.
  *   - Errors in arguments return at once and launch nothing; a failed launch
  *     returns MR_ERR_CUDA.  mr_last_error() then describes the failure.
  *   - Allowed aliasing (in place) is listed per call; any other overlap between
