@@ -298,8 +298,8 @@ mr_status_t run_reduce(const char* what, int mode, const void* const* send, void
     for (int p = 0; p < W; p += P.group) P.gmask |= 1ull << p;
     P.nseg = algo == MR_HIER ? plan_segments_hier(W, N, group, mode == mr::MODE_REDUCE_SCATTER, P.seg)
                              : plan_segments(W, N, algo, P.seg);
-    const int vb = mr::reduce_vector_bytes(W, algo);
     const int eb = (int)elem_bytes(dtype);
+    const int vb = mr::reduce_vector_bytes(W, algo, eb);
     bool vec = true;
     for (int r = 0; r < W; ++r)
         vec = vec && ((uintptr_t)send[r] % vb == 0) && ((uintptr_t)recv[r] % vb == 0);
@@ -524,7 +524,7 @@ mr_status_t mr_allreduce_rmsnorm(const void* const* send, void* const* recv, int
     P.W = W;
     P.eps = eps;
     P.nseg = plan_segments(W, N, algo, P.seg);
-    const int vb = mr::reduce_vector_bytes(W, MR_TREE);     // the norm kernel narrows beyond 16 ranks
+    const int vb = mr::norm_vector_bytes(W);
     const size_t lanes = vb / b;
     bool vec = hidden % lanes == 0;
     for (int r = 0; r < W; ++r) vec = vec && ((uintptr_t)send[r] % vb == 0) && ((uintptr_t)recv[r] % vb == 0);

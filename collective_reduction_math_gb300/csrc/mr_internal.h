@@ -109,14 +109,29 @@ struct GatherParams {
 // vector per W loads, and at W = 8 runs faster with two vectors per thread at
 // 2 CTAs per SM (measured on GB300: 6.8 against 5.8 TB/s).
 constexpr int reduce_wcap(int W) { return W <= 2 ? 2 : W <= 4 ? 4 : W <= 8 ? 8 : W <= 16 ? 16 : 64; }
-// Above 16 ranks the tree keeps all W values in registers and so narrows its
-// vectors to 4 bytes; the left-fold orders fold in batches of 8 and keep 16.
-constexpr int reduce_vector_bytes(int W, int algo) { return (W <= 16 || algo != MR_TREE) ? 16 : 4; }
+// Above 16 ranks every order folds the ranks in batches of 8 with 16-byte
+// vectors, except the tree on bf16, which takes 8-byte vectors (4 lanes) so
+// that the per-batch partials of all 8 batches fit in registers.
+constexpr int reduce_vector_bytes(int W, int algo, int elem_bytes) {
+    return (W <= 16 || algo != MR_TREE || elem_bytes == 4) ? 16 : 8;
+}
+// The fused RMSNorm kernel keeps all W values of a lane in registers and so
+// narrows its vectors to 4 bytes above 16 ranks.
+constexpr int norm_vector_bytes(int W) { return W <= 16 ? 16 : 4; }
 constexpr int reduce_unroll_for(int wcap, bool rs) {
     return wcap == 2 ? 4 : wcap == 4 ? 2 : (wcap == 8 && rs) ? 2 : 1;
 }
 constexpr int reduce_unroll(int W, bool rs) { return reduce_unroll_for(reduce_wcap(W), rs); }
 constexpr int reduce_blocks_per_sm(int wcap, int u) { return (wcap <= 8 && wcap * u <= 8) ? 3 : 2; }
+// 13 to 16 ranks fold in batches of 8 (as above 16 ranks), which frees the
+// registers that 16 live vectors and 16 pointers take; measured on GB300 at
+// W = 16 (TB/s, plain -> batched): fp32 ring 5.4 -> 6.2, fp32 tree 6.3 -> 6.5,
+// bf16 tree 4.8 -> 6.4, int32 tree 5.8 -> 6.0, rings otherwise within 2 %.
+// At W = 12 the second batch is half empty and the plain fold stays ahead,
+// and per-hop bf16 sum / avg keeps the plain fold's packed bf16x2 pairs.
+constexpr bool reduce_batched16(int dtype, int op, bool hop) {
+    return !(dtype == MR_BF16 && hop && (op == MR_SUM || op == MR_AVG));
+}
 
 // ---------------------------------------------------------------------------
 // Programmatic dependent launch.  Every kernel of the library is launched with

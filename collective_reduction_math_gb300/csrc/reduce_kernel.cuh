@@ -25,6 +25,7 @@
 
 #include <cuda_bf16.h>
 #include <stdint.h>
+#include <string.h>
 
 #include <type_traits>
 
@@ -109,6 +110,26 @@ template <int DT, int OP> struct Arith {
     }
 };
 
+// Per-hop bf16 sums on packed pairs.  With per-hop rounding a bf16 sum or avg
+// adds two bf16 values in fp32 and rounds the result to bf16 at every hop.
+// fp32 carries 24 significant bits, at least 2*8+1 for bf16's 8, so that
+// double rounding equals the single correctly rounded bf16 sum (and below
+// fp32's normal range the fp32 sum of two bf16 values is exact); one packed
+// bf16x2 add therefore does two lanes' hop at once, with the same result.
+struct Bf16PairSum {
+    using acc_t = uint32_t;
+    static __device__ __forceinline__ acc_t combine(acc_t a, acc_t b) {
+        __nv_bfloat162 x, y;
+        memcpy(&x, &a, 4);
+        memcpy(&y, &b, 4);
+        const __nv_bfloat162 r = __hadd2(x, y);
+        acc_t o;
+        memcpy(&o, &r, 4);
+        return o;
+    }
+    static __device__ __forceinline__ acc_t hop(acc_t a) { return a; }
+};
+
 // ---------------------------------------------------------------------------
 // The folds.  y[p] holds the contribution at order position p; only the
 // first W positions are valid.  All register indices are compile-time.
@@ -164,6 +185,36 @@ __device__ __forceinline__ typename A::acc_t fold_tree(typename A::acc_t (&y)[WC
         }
     }
     return a;
+}
+
+// The in-batch part of the tree fold for more than 16 ranks.  Positions come
+// in batches of 8, [8m, 8m+8); positions 8m+1 .. 8m+7 lie in whole subtrees
+// of the batch (the subtree of a node at level b spans (p-b, p+b)), so the
+// levels 2 and 4 of a batch fold on their own (y[0] is the batch head, at
+// level 8 or above).  Returns the subtotal of the node that the head's
+// upper-child search finds inside the batch: the largest h in {4, 2, 1}
+// with h < Wb (valid when Wb >= 2).
+template <class A>
+__device__ __forceinline__ typename A::acc_t tree_batch_top(typename A::acc_t (&y)[8], int Wb, bool hop) {
+#pragma unroll
+    for (int b = 2; b < 8; b <<= 1) {
+#pragma unroll
+        for (int p = b; p < 8; p += 2 * b) {
+            if (p < Wb) {
+                typename A::acc_t a = comb<A>(y[p], y[p - b / 2], hop);
+                bool taken = false;
+#pragma unroll
+                for (int h = b / 2; h >= 1; h >>= 1) {
+                    if (!taken && p + h < Wb) {
+                        a = comb<A>(a, y[p + h], hop);
+                        taken = true;
+                    }
+                }
+                y[p] = a;
+            }
+        }
+    }
+    return Wb > 4 ? y[4] : Wb > 2 ? y[2] : y[1];
 }
 
 // Hierarchical: positions come group by group (gmask marks the first position
@@ -321,7 +372,7 @@ __device__ __forceinline__ int order_rank(int W, const Segment& sg, int i, int g
     else return hier_rank(W, group, sg.hc, sg.hd, i);
 }
 
-template <int DT, int OP, int ALGO, int WCAP, int VB, int U, bool HOP>
+template <int DT, int OP, int ALGO, int WCAP, int VB, int U, bool HOP, bool BATCH>
 __global__ void __launch_bounds__(kThreads, reduce_blocks_per_sm(WCAP, U))
 reduce_kernel(const __grid_constant__ ReduceParams P) {
     using A = Arith<DT, OP>;
@@ -336,6 +387,8 @@ reduce_kernel(const __grid_constant__ ReduceParams P) {
     const float s = P.scale;
     const bool rs = (P.mode == MODE_REDUCE_SCATTER);
     constexpr bool hop = DT == MR_BF16 && HOP;
+    // per-hop bf16 sum / avg: fold two lanes per packed word (Bf16PairSum)
+    constexpr bool kPairs = hop && (OP == MR_SUM || OP == MR_AVG) && VB == 16;
     const uint64_t gmask = P.gmask;
     // a contribution as read: widened, pre-scaled, and for per-hop bf16 rounded
     auto contrib = [&](raw_t x) -> acc_t {
@@ -345,8 +398,12 @@ reduce_kernel(const __grid_constant__ ReduceParams P) {
 
     // Input pointers in the current segment's accumulation order: in
     // registers for up to 16 ranks, in a shared-memory table beyond that.
-    constexpr bool kTable = WCAP > 16;
-    constexpr bool kBatched = WCAP > 16 && ALGO != MR_TREE;
+    // BATCH: the ranks are loaded and folded in batches of 8 (only 8 vectors
+    // live at a time), and the pointer table sits in shared memory.
+    constexpr bool kTable = BATCH;
+    constexpr bool kBatched = BATCH && ALGO != MR_TREE;
+    constexpr bool kTreeBatched = BATCH && ALGO == MR_TREE;
+    static_assert(!BATCH || WCAP % 8 == 0, "batches of 8 positions");
     __shared__ const char* table[kTable ? WCAP : 1];
     const char* src[kTable ? 1 : WCAP];
     int cur = -1;
@@ -403,11 +460,12 @@ reduce_kernel(const __grid_constant__ ReduceParams P) {
             const uint64_t va = (sg.lo + LANES - 1) / LANES, vb = sg.hi / LANES;
             const uint64_t v0 = va + local * kTile + threadIdx.x;
             if constexpr (kBatched) {
-                // More than 16 ranks in a left-fold order (ring, hierarchical):
+                // A left-fold order (ring, hierarchical) over many ranks:
                 // the ranks come in batches of 8 (8 independent 16-byte loads
                 // in flight, as at W = 8) and the fold's state -- the running
                 // group part and the total of the groups so far -- carries
                 // from batch to batch.  Same order, same operations.
+                static_assert(U == 1, "the batched folds take one vector per thread per tile");
                 if (v0 < vb) {
                     const uint64_t off = v0 * VB;
                     acc_t part[LANES], total[LANES];
@@ -458,6 +516,88 @@ reduce_kernel(const __grid_constant__ ReduceParams P) {
                 }
                 continue;
             }
+            if constexpr (kTreeBatched) {
+                // The tree order over many ranks: each batch of 8
+                // positions is loaded (8 vectors in flight) and folded up to
+                // its in-batch top node (tree_batch_top), keeping per batch
+                // only the head's own value and that subtotal.  The heads 8m
+                // then form the same bit-trick tree over m (level = lowest set
+                // bit of m): a head takes its own value, then its lower child
+                // (the previous batch's top for m odd, else head m - B/2), then
+                // its upper child (head m + h for the largest h in {B/2, ..., 1}
+                // below the number of heads, else its own batch's top).  The
+                // root takes its one child.  These are fold_tree's combines in
+                // fold_tree's order.
+                static_assert(U == 1, "the batched folds take one vector per thread per tile");
+                constexpr int NB = WCAP / 8;      // batches of 8 positions
+                if (v0 < vb) {
+                    const uint64_t off = v0 * VB;
+                    const int M = (W + 7) >> 3;
+                    acc_t head[NB][LANES], top[NB][LANES];
+#pragma unroll
+                    for (int m = 0; m < NB; ++m) {
+                        if (m < M) {
+                            const int Wb = min(8, W - 8 * m);
+                            Vec<VB> raw[8];
+#pragma unroll
+                            for (int q = 0; q < 8; ++q)
+                                if (q < Wb) raw[q] = load_vec<VB>(input(8 * m + q) + off);
+#pragma unroll
+                            for (int l = 0; l < LANES; ++l) {
+                                acc_t y[8];
+#pragma unroll
+                                for (int q = 0; q < 8; ++q)
+                                    if (q < Wb) y[q] = contrib(get_lane<raw_t, VB>(raw[q], l));
+                                head[m][l] = y[0];
+                                top[m][l] = tree_batch_top<A>(y, Wb, hop);
+                            }
+                        }
+                    }
+#pragma unroll
+                    for (int B = 1; B < NB; B <<= 1) {
+#pragma unroll
+                        for (int m = B; m < NB; m += 2 * B) {
+                            if (m < M) {
+#pragma unroll
+                                for (int l = 0; l < LANES; ++l) {
+                                    acc_t a = comb<A>(head[m][l], B == 1 ? top[m - 1][l] : head[m - B / 2][l], hop);
+                                    bool taken = false;
+#pragma unroll
+                                    for (int h = B / 2; h >= 1; h >>= 1) {
+                                        if (!taken && m + h < M) {
+                                            a = comb<A>(a, head[m + h][l], hop);
+                                            taken = true;
+                                        }
+                                    }
+                                    if (!taken && 8 * m + 1 < W) a = comb<A>(a, top[m][l], hop);
+                                    head[m][l] = a;
+                                }
+                            }
+                        }
+                    }
+                    Vec<VB> res;
+#pragma unroll
+                    for (int l = 0; l < LANES; ++l) {
+                        acc_t a = head[0][l];
+                        bool taken = false;
+#pragma unroll
+                        for (int h = NB / 2; h >= 1; h >>= 1) {
+                            if (!taken && h < M) {
+                                a = comb<A>(a, head[h][l], hop);
+                                taken = true;
+                            }
+                        }
+                        set_lane<raw_t, VB>(res, l, A::post(a, W));
+                    }
+                    if (rs) {
+                        store_vec<VB>(static_cast<char*>(P.out[sg.k]) + off - sg.out_lo * EB, res);
+                    } else {
+#pragma unroll 8
+                        for (int j = 0; j < W; ++j) store_vec<VB>(static_cast<char*>(P.out[j]) + off, res);
+                    }
+                }
+                continue;
+            }
             // U*W independent 16-byte loads in flight before the first fold.
             Vec<VB> raw[U][WCAP];
 #pragma unroll
@@ -475,10 +615,37 @@ reduce_kernel(const __grid_constant__ ReduceParams P) {
                 if (v >= vb) break;
                 const uint64_t off = v * VB;
                 Vec<VB> res;
-                acc_t r[LANES];
-                fold_lanes<A, ALGO, WCAP, VB, LANES>(raw[u], W, gmask, hop, contrib, r);
+                if constexpr (kPairs) {
+                    // each word: two bf16 contributions, as read (avg:
+                    // pre-scaled in fp32 and rounded to bf16 per lane)
+                    auto pair = [&](uint32_t w) -> uint32_t {
+                        if constexpr (OP == MR_AVG) {
+                            // widen, pre-scale in fp32, round both lanes to
+                            // bf16 in one packed conversion (lo lane in x)
+                            const float lo = __fmul_rn(__uint_as_float(w << 16), s);
+                            const float hi = __fmul_rn(__uint_as_float(w & 0xFFFF0000u), s);
+                            const __nv_bfloat162 p = __floats2bfloat162_rn(lo, hi);
+                            uint32_t o;
+                            memcpy(&o, &p, 4);
+                            return o;
+                        } else {
+                            return w;
+                        }
+                    };
 #pragma unroll
-                for (int l = 0; l < LANES; ++l) set_lane<raw_t, VB>(res, l, A::post(r[l], W));
+                    for (int k = 0; k < VB / 4; ++k) {
+                        uint32_t y[WCAP];
+#pragma unroll
+                        for (int i = 0; i < WCAP; ++i)
+                            if (i < W) y[i] = pair(raw[u][i].w[k]);
+                        res.w[k] = fold<Bf16PairSum, ALGO, WCAP>(y, W, false, gmask);
+                    }
+                } else {
+                    acc_t r[LANES];
+                    fold_lanes<A, ALGO, WCAP, VB, LANES>(raw[u], W, gmask, hop, contrib, r);
+#pragma unroll
+                    for (int l = 0; l < LANES; ++l) set_lane<raw_t, VB>(res, l, A::post(r[l], W));
+                }
                 if (rs) {
                     store_vec<VB>(static_cast<char*>(P.out[sg.k]) + off - sg.out_lo * EB, res);
                 } else {
@@ -521,14 +688,20 @@ cudaError_t launch_reduce(const ReduceParams& P, int op, dim3 grid, cudaStream_t
         constexpr int OP = decltype(op_c)::value;
         const bool rs = P.mode == MODE_REDUCE_SCATTER;
         switch (reduce_wcap(P.W)) {
-            case 2: return launch_kernel(reduce_kernel<DT, OP, ALGO, 2, 16, reduce_unroll_for(2, false), HOP>, grid, 0, stream, 0, P);
-            case 4: return launch_kernel(reduce_kernel<DT, OP, ALGO, 4, 16, reduce_unroll_for(4, false), HOP>, grid, 0, stream, 0, P);
+            case 2: return launch_kernel(reduce_kernel<DT, OP, ALGO, 2, 16, reduce_unroll_for(2, false), HOP, false>, grid, 0, stream, 0, P);
+            case 4: return launch_kernel(reduce_kernel<DT, OP, ALGO, 4, 16, reduce_unroll_for(4, false), HOP, false>, grid, 0, stream, 0, P);
             case 8:
-                if (rs) return launch_kernel(reduce_kernel<DT, OP, ALGO, 8, 16, reduce_unroll_for(8, true), HOP>, grid, 0, stream, 0, P);
-                return launch_kernel(reduce_kernel<DT, OP, ALGO, 8, 16, reduce_unroll_for(8, false), HOP>, grid, 0, stream, 0, P);
-            case 16: return launch_kernel(reduce_kernel<DT, OP, ALGO, 16, 16, reduce_unroll_for(16, false), HOP>, grid, 0, stream, 0, P);
+                if (rs) return launch_kernel(reduce_kernel<DT, OP, ALGO, 8, 16, reduce_unroll_for(8, true), HOP, false>, grid, 0, stream, 0, P);
+                return launch_kernel(reduce_kernel<DT, OP, ALGO, 8, 16, reduce_unroll_for(8, false), HOP, false>, grid, 0, stream, 0, P);
+            case 16:
+                if constexpr (reduce_batched16(DT, OP, HOP)) {
+                    if (P.W > 12)
+                        return launch_kernel(reduce_kernel<DT, OP, ALGO, 16, 16, 1, HOP, true>, grid, 0, stream, 0, P);
+                }
+                return launch_kernel(reduce_kernel<DT, OP, ALGO, 16, 16, reduce_unroll_for(16, false), HOP, false>, grid, 0, stream, 0, P);
             default:
-                return launch_kernel(reduce_kernel<DT, OP, ALGO, 64, reduce_vector_bytes(64, ALGO), reduce_unroll_for(64, false), HOP>,
+                return launch_kernel(reduce_kernel<DT, OP, ALGO, 64, reduce_vector_bytes(64, ALGO, Elem<DT>::kBytes),
+                                                   reduce_unroll_for(64, false), HOP, true>,
                                      grid, 0, stream, 0, P);
         }
     };

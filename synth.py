@@ -66,6 +66,23 @@ def near_one(seed: int, W: int, N: int, dtype: str = "fp32", tag: int = TAG_GRAD
     return out
 
 
+def bf16_wide(seed: int, W: int, N: int, tag: int = TAG_GRAD):
+    """W buffers of N bf16 bit patterns spread over the whole exponent range
+    below 2^73 (so sums of up to 64 stay finite): random sign and mantissa,
+    exponent field uniform in [0, 200], one in eight subnormal (field 0).
+    Sums of such values span gaps far wider than fp32's precision and land
+    on bf16 ties, the cases where rounding order matters."""
+    out = []
+    for r in range(W):
+        g = _rng(seed, tag, r)
+        sign = g.integers(0, 2, size=N, dtype=np.uint16) << 15
+        mant = g.integers(0, 128, size=N, dtype=np.uint16)
+        expo = g.integers(1, 201, size=N, dtype=np.uint16)
+        expo[g.integers(0, 8, size=N) == 0] = 0
+        out.append((sign | (expo << 7) | mant).astype(np.uint16))
+    return out
+
+
 def random_values(seed: int, W: int, N: int, dtype: str, kind: str = "normal", tag: int = TAG_GRAD):
     """Generic test data.  int32: uniform in [-1000, 1000].  Floats: 'normal'
     (sigma 1), 'small_int' (integers in [-8, 8]) or 'near_one' ([0.5, 1.5))."""

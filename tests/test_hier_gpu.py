@@ -57,13 +57,45 @@ def test_hier_parity(mr, W, group, dtype):
 
 
 @pytest.mark.parametrize("algo,group", [("ring", None), ("tree", None), ("hier", 4)])
-@pytest.mark.parametrize("W", [2, 8, 16])
+@pytest.mark.parametrize("W", [2, 8, 16, 40])
 def test_per_hop_bf16_parity(mr, algo, group, W):
     if algo == "hier" and W % 4:
         group = 2
     for N in (W * 4096 + 24, 7 * W):
         for op in ("sum", "avg", "min"):
             check(mr, "bf16", op, algo, group, True, W, N)
+
+
+@pytest.mark.parametrize("algo,group", [("ring", None), ("tree", None), ("hier", 4)])
+@pytest.mark.parametrize("W", [3, 8, 16, 40])
+def test_per_hop_bf16_wide_values(mr, algo, group, W):
+    """Per-hop bf16 sum and avg on values spread over the whole exponent range,
+    subnormals included: every hop's rounding decides the result, so a kernel
+    that rounded differently from the oracle's fp32-add-then-round would
+    differ somewhere in these buffers."""
+    import oracle
+    import torch
+    if algo == "hier" and W % 4:
+        group = 3 if W % 3 == 0 else 2
+    for N in (W * 8192 + 40, 9 * W):
+        host = synth.bf16_wide(740 + W, W, N)
+        xs = [to_device(h, "bf16") for h in host]
+        for op in ("sum", "avg"):
+            g = Guarded(W, N, "bf16")
+            mr.mr_allreduce_ex(xs, g.views, op=op, algo=algo, group=group, per_hop=True)
+            torch.cuda.synchronize()
+            g.check()
+            want = oracle.allreduce_ex("bf16", op, algo, host, group=group or 0, hop=True)
+            for j, o in enumerate(g.host()):
+                assert_same(o, want, f"per-hop wide {op} {algo} W={W} N={N} rank {j}")
+            if N % W == 0:
+                sh = Guarded(W, N // W, "bf16")
+                mr.mr_reduce_scatter_ex(xs, sh.views, op=op, algo=algo, group=group, per_hop=True)
+                torch.cuda.synchronize()
+                sh.check()
+                want_rs = oracle.reduce_scatter_ex("bf16", op, algo, host, group=group or 0, hop=True)
+                for k, o in enumerate(sh.host()):
+                    assert_same(o, want_rs[k], f"per-hop wide rs {op} {algo} W={W} shard {k}")
 
 
 def test_ex_defaults_match_plain(mr):
