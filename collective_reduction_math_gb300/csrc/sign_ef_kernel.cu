@@ -12,10 +12,11 @@
 //   sign_l1_kernel      per-block partial L1 norms of p into a workspace:
 //                       each thread a compensated (Neumaier) fp32 sum over
 //                       its elements, then an fp64 tree over the block;
-//   sign_ef_kernel      every CTA first sums each rank's partials in block
-//                       order in fp64 and rounds s_r = sum / N once to fp32
-//                       (CTA 0 also writes the scales out); then decode,
-//                       error update and reduction in one pass.
+//   sign_ef_kernel      every CTA first sums each rank's partials in fp64 in
+//                       one fixed order (a warp per rank) and rounds
+//                       s_r = sum / N once to fp32 (CTA 0 also writes the
+//                       scales out); then decode, error update and
+//                       reduction in one pass.
 // HBM bytes: the first kernel reads g and e (2 W N 4); the second reads them
 // again, writes e (W N 4) and the output (W N 4 for all-reduce, N 4 for
 // reduce-scatter).
@@ -88,12 +89,23 @@ sign_ef_kernel(const __grid_constant__ SignParams P) {
 
     const int W = P.W;
     const bool rs = (P.mode == MODE_REDUCE_SCATTER);
-    if (threadIdx.x < W) {
-        double S = 0.0;
-        for (int b = 0; b < P.nb; ++b) S = __dadd_rn(S, P.partials[(uint64_t)threadIdx.x * P.nb + b]);
-        const float sc = __double2float_rn(__ddiv_rn(S, (double)P.N));
-        scale[threadIdx.x] = sc;
-        if (blockIdx.x == 0 && P.scales) P.scales[threadIdx.x] = sc;
+    // The scales: one warp per rank; lane j adds partials j, j+32, ... in
+    // order, then a fixed butterfly over the lanes, read from lane 0 (the
+    // same order on every CTA and every run).  All of a lane's loads are
+    // independent, so this costs one round trip rather than nb.
+    {
+        const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+        for (int r = warp; r < W; r += kThreads / 32) {
+            double S = 0.0;
+            for (int b = lane; b < P.nb; b += 32) S = __dadd_rn(S, P.partials[(uint64_t)r * P.nb + b]);
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) S = __dadd_rn(S, __shfl_xor_sync(0xffffffffu, S, o));
+            if (lane == 0) {
+                const float sc = __double2float_rn(__ddiv_rn(S, (double)P.N));
+                scale[r] = sc;
+                if (blockIdx.x == 0 && P.scales) P.scales[r] = sc;
+            }
+        }
     }
     __syncthreads();
 
