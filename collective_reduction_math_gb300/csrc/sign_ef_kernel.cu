@@ -140,13 +140,28 @@ sign_ef_kernel(const __grid_constant__ SignParams P) {
 
     if (P.vec) {
         // Vector tiles dealt round-robin across the segments, as in the
-        // all-reduce kernel.
+        // all-reduce kernel.  Per order position, the rank's scale s and the
+        // share a decoded value contributes (s, or s * fl32(1/W) for avg; the
+        // sign is applied after, which IEEE multiplication allows exactly)
+        // are kept in registers while the CTA stays on one segment.
+        float sc[WCAP], sh[WCAP];
+        int cur = -1;
         const uint64_t ntiles = P.tiles_max * (uint64_t)P.nseg;
         for (uint64_t t = blockIdx.x; t < ntiles; t += gridDim.x) {
             const int seg = (int)(t % (uint64_t)P.nseg);
             const uint64_t local = t / (uint64_t)P.nseg;
             if (local >= P.tile_start[seg + 1] - P.tile_start[seg]) continue;
             const Segment& sg = P.seg[seg];
+            if (seg != cur) {
+                cur = seg;
+#pragma unroll
+                for (int i = 0; i < WCAP; ++i) {
+                    if (i < W) {
+                        sc[i] = scale[order_rank<ALGO>(W, sg, i)];
+                        sh[i] = OP == MR_AVG ? __fmul_rn(sc[i], P.avg) : sc[i];
+                    }
+                }
+            }
             const uint64_t va = (sg.lo + LANES - 1) / LANES, vb = sg.hi / LANES;
             const uint64_t v = va + local * kThreads + threadIdx.x;
             if (v >= vb) continue;
@@ -167,10 +182,11 @@ sign_ef_kernel(const __grid_constant__ SignParams P) {
 #pragma unroll
                 for (int i = 0; i < WCAP; ++i) {
                     if (i < W) {
-                        float en;
-                        y[i] = decode(order_rank<ALGO>(W, sg, i), __uint_as_float(gv[i].w[l]),
-                                      __uint_as_float(ev[i].w[l]), &en);
-                        ev[i].w[l] = __float_as_uint(en);
+                        // the decode above, with the scales from registers
+                        const float p = __fadd_rn(__uint_as_float(gv[i].w[l]), __uint_as_float(ev[i].w[l]));
+                        const bool pos = p >= 0.0f;
+                        ev[i].w[l] = __float_as_uint(__fsub_rn(p, pos ? sc[i] : -sc[i]));
+                        y[i] = pos ? sh[i] : -sh[i];
                     }
                 }
                 res.w[l] = A::post(fold<A, ALGO, WCAP>(y, W), W);
