@@ -9,15 +9,19 @@
 // C > 1 spreads one row over several SMs; with many rows C = 1.
 //   pass 1  for every element: reduce the W contributions exactly as the
 //           all-reduce kernel does (same chunks, same ring or tree order,
-//           fp32), add the residual (one fp32 add), write the rounded h to
-//           residual_out, keep the fp32 h in shared memory, and accumulate
-//           h*h into a per-thread fp32 partial (increasing element order);
+//           fp32), add the residual (one fp32 add), keep the fp32 h in
+//           shared memory, and accumulate h*h into a per-thread fp32
+//           partial (increasing element order);
 //   reduce  the partials with a fixed tree (warp shuffles, then the warp
 //           totals), then the C slice totals in cluster-rank order, read
 //           from each CTA's shared memory over the cluster (DSMEM), so every
 //           CTA -- and every run -- gets the same value;
 //           inv = 1 / sqrt(ss / hidden + eps), each step one IEEE operation;
-//   pass 2  out = (h * inv) * weight, rounded once, stored to all W outputs.
+//   pass 2  out = (h * inv) * weight, rounded once, stored to all W outputs;
+//           residual_out gets h rounded once, from the same fp32 h.  Pass 1
+//           stores nothing to global memory, so the cluster barrier between
+//           the passes has no stores to wait for, and each thread's first
+//           weight vector is loaded once, before the first row.
 // Bytes per row: W reads and W writes of the row, plus the residual read,
 // residual_out write and weight read (the weight stays in L2 across rows).
 #include <cooperative_groups.h>
@@ -78,9 +82,13 @@ allreduce_rmsnorm_kernel(const __grid_constant__ NormParams P) {
             if (i < W) y[i] = A::read(__ldg(reinterpret_cast<const raw_t*>(input(sg, i)) + e), 0.0f);
         float h = fold<A, ALGO, WCAP>(y, W);
         if (P.residual) h = __fadd_rn(h, A::read(__ldg(static_cast<const raw_t*>(P.residual) + e), 0.0f));
-        if (P.residual_out) static_cast<raw_t*>(P.residual_out)[e] = A::post(h, W);
         return h;
     };
+
+    // This thread's first pass-2 weight vector: the same for every row.
+    Vec<VB> w_first;
+    if (P.vec && v_lo + threadIdx.x < v_hi)
+        w_first = load_vec<VB>(static_cast<const char*>(P.weight) + (v_lo + threadIdx.x) * VB);
 
     int parity = 0;
     for (uint64_t row = first_row; row < P.rows; row += row_stride, parity ^= 1) {
@@ -103,7 +111,6 @@ allreduce_rmsnorm_kernel(const __grid_constant__ NormParams P) {
                         if (i < W) raw[i] = load_vec<VB>(input(sg, i) + e0 * EB);
                     Vec<VB> rv;
                     if (P.residual) rv = load_vec<VB>(static_cast<const char*>(P.residual) + e0 * EB);
-                    Vec<VB> ro;
 #pragma unroll
                     for (int l = 0; l < LANES; ++l) {
                         float y[WCAP];
@@ -113,9 +120,7 @@ allreduce_rmsnorm_kernel(const __grid_constant__ NormParams P) {
                         float h = fold<A, ALGO, WCAP>(y, W);
                         if (P.residual) h = __fadd_rn(h, A::read(get_lane<raw_t, VB>(rv, l), 0.0f));
                         hv[l] = h;
-                        set_lane<raw_t, VB>(ro, l, A::post(h, W));
                     }
-                    if (P.residual_out) store_vec<VB>(static_cast<char*>(P.residual_out) + e0 * EB, ro);
                 } else {
                     // the vector straddles a chunk (or tree) boundary
 #pragma unroll
@@ -189,13 +194,20 @@ allreduce_rmsnorm_kernel(const __grid_constant__ NormParams P) {
 #pragma unroll
                     for (int l = 0; l < LANES; ++l) hv[l] = hs[sv * LANES + l];
                 }
-                const Vec<VB> wv = load_vec<VB>(static_cast<const char*>(P.weight) + v * VB);
+                const Vec<VB> wv = (v == v_lo + threadIdx.x) ? w_first
+                                                              : load_vec<VB>(static_cast<const char*>(P.weight) + v * VB);
                 Vec<VB> o;
 #pragma unroll
                 for (int l = 0; l < LANES; ++l)
                     set_lane<raw_t, VB>(o, l, A::post(__fmul_rn(__fmul_rn(hv[l], inv),
                                                                 A::read(get_lane<raw_t, VB>(wv, l), 0.0f)), W));
                 const uint64_t off = (base + v * LANES) * EB;
+                if (P.residual_out) {
+                    Vec<VB> ro;
+#pragma unroll
+                    for (int l = 0; l < LANES; ++l) set_lane<raw_t, VB>(ro, l, A::post(hv[l], W));
+                    store_vec<VB>(static_cast<char*>(P.residual_out) + off, ro);
+                }
 #pragma unroll
                 for (int j = 0; j < WCAP; ++j)
                     if (j < W) store_vec<VB>(static_cast<char*>(P.out[j]) + off, o);
@@ -203,6 +215,7 @@ allreduce_rmsnorm_kernel(const __grid_constant__ NormParams P) {
         } else {
             for (uint64_t i = c_lo + threadIdx.x; i < c_hi; i += kThreads) {
                 const float w = A::read(__ldg(static_cast<const raw_t*>(P.weight) + i), 0.0f);
+                if (P.residual_out) static_cast<raw_t*>(P.residual_out)[base + i] = A::post(hs[i - c_lo], W);
                 const raw_t o = A::post(__fmul_rn(__fmul_rn(hs[i - c_lo], inv), w), W);
 #pragma unroll
                 for (int j = 0; j < WCAP; ++j)
@@ -211,8 +224,10 @@ allreduce_rmsnorm_kernel(const __grid_constant__ NormParams P) {
         }
         __syncthreads();    // the row buffer and the partials are reused by the next row
     }
-    // Peers may still read this CTA's slice totals: leave together.
-    if (C > 1) cluster.sync();
+    // Peers may still read this CTA's slice totals: leave together.  Each
+    // peer has consumed what it read before it arrives, so the arrive need
+    // not wait for this CTA's output stores (relaxed).
+    if (C > 1) asm volatile("barrier.cluster.arrive.relaxed.aligned;\n\tbarrier.cluster.wait.aligned;" ::: "memory");
 }
 
 template <int DT, int ALGO, int WCAP, int VB>
