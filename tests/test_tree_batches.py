@@ -1,0 +1,101 @@
+"""The tree order folded in batches of 8 positions gives exactly the oracle's
+tree fold.
+
+From 13 ranks up the CUDA kernel does not hold all W contributions of an
+element at once.  It loads the positions in batches [8m, 8m+8), folds each
+batch up to the node that the batch head's upper-child search finds inside it,
+and then folds the batch heads 8m as the same bit-trick tree one level up.
+This test restates that schedule on symbols and checks, for every W from 9 to
+64, that it performs the oracle's combines in the oracle's order: each node's
+own value first, then its children's subtotals in the order the oracle lists
+them (double binary tree, "The double binary tree", post on NCCL all-reduce).
+Positions, not ranks, are folded, so one check covers both trees.
+"""
+import pytest
+
+
+def oracle_fold(W, oracle_mod):
+    """The symbolic fold of tree 1 over positions, from the oracle's tree."""
+    root, _parent, kids = oracle_mod.tree(W, 1)
+
+    def sub(v):
+        e = f"y{v}"
+        for c in kids[v]:
+            e = f"({e}+{sub(c)})"
+        return e
+    return sub(root)
+
+
+def batch_top(yb, Wb):
+    """Levels 2 and 4 inside one batch (yb[0] is the head), then the subtotal
+    of the largest h in {4, 2, 1} with h < Wb."""
+    y = list(yb)
+    b = 2
+    while b < 8:
+        for p in range(b, 8, 2 * b):
+            if p < Wb:
+                a = f"({y[p]}+{y[p - b // 2]})"
+                h = b // 2
+                while h >= 1:
+                    if p + h < Wb:
+                        a = f"({a}+{y[p + h]})"
+                        break
+                    h //= 2
+                y[p] = a
+        b *= 2
+    for h in (4, 2, 1):
+        if h < Wb:
+            return y[h]
+    return None
+
+
+def batched_fold(W, slots, swap_children=False):
+    """The kernel's schedule with `slots` register slots (16 or 64).
+    swap_children plants a mistake: a head adds its upper child first."""
+    y = [f"y{i}" for i in range(W)] + [None] * (slots + 8 - W)
+    NB, M = slots // 8, (W + 7) // 8
+    head, top = [None] * NB, [None] * NB
+    for m in range(min(NB, M)):
+        Wb = min(8, W - 8 * m)
+        head[m] = y[8 * m]
+        top[m] = batch_top(y[8 * m:8 * m + 8], Wb)
+    B = 1
+    while B < NB:
+        for m in range(B, NB, 2 * B):
+            if m < M:
+                lower = top[m - 1] if B == 1 else head[m - B // 2]
+                upper = None
+                h = B // 2
+                while h >= 1:
+                    if m + h < M:
+                        upper = head[m + h]
+                        break
+                    h //= 2
+                if upper is None and 8 * m + 1 < W:
+                    upper = top[m]
+                first, second = (upper, lower) if swap_children and upper is not None else (lower, upper)
+                a = f"({head[m]}+{first})"
+                if second is not None:
+                    a = f"({a}+{second})"
+                head[m] = a
+        B *= 2
+    a, h = head[0], NB // 2
+    while h >= 1:
+        if h < M:
+            return f"({a}+{head[h]})"
+        h //= 2
+    return a
+
+
+@pytest.mark.parametrize("W", range(9, 65))
+def test_batched_tree_is_the_oracle_tree(oracle_mod, W):
+    slots = 16 if W <= 16 else 64
+    assert batched_fold(W, slots) == oracle_fold(W, oracle_mod)
+
+
+@pytest.mark.parametrize("W", [12, 24, 64])
+def test_a_planted_mistake_is_caught(oracle_mod, W):
+    """A head that adds its upper child before its lower one is caught."""
+    slots = 16 if W <= 16 else 64
+    assert batched_fold(W, slots) == oracle_fold(W, oracle_mod)
+    assert batched_fold(W, slots, swap_children=True) != oracle_fold(W, oracle_mod)
