@@ -109,11 +109,17 @@ struct GatherParams {
 // vector per W loads, and at W = 8 runs faster with two vectors per thread at
 // 2 CTAs per SM (measured on GB300: 6.8 against 5.8 TB/s).
 constexpr int reduce_wcap(int W) { return W <= 2 ? 2 : W <= 4 ? 4 : W <= 8 ? 8 : W <= 16 ? 16 : 64; }
+// Per-hop bf16 sum and avg fold packed pairs (two lanes per 32-bit word).
+constexpr bool reduce_pairs(int dtype, int op, bool hop) {
+    return dtype == MR_BF16 && hop && (op == MR_SUM || op == MR_AVG);
+}
 // Above 16 ranks every order folds the ranks in batches of 8 with 16-byte
-// vectors, except the tree on bf16, which takes 8-byte vectors (4 lanes) so
-// that the per-batch partials of all 8 batches fit in registers.
-constexpr int reduce_vector_bytes(int W, int algo, int elem_bytes) {
-    return (W <= 16 || algo != MR_TREE || elem_bytes == 4) ? 16 : 8;
+// vectors, except the tree on bf16 lanes unpacked to fp32, which takes 8-byte
+// vectors (4 lanes) so that the per-batch partials of all 8 batches fit in
+// registers.  The host's alignment check and the kernel's template both take
+// the width from here.
+constexpr int reduce_vector_bytes(int W, int algo, int dtype, int op, bool hop) {
+    return (W <= 16 || algo != MR_TREE || dtype != MR_BF16 || reduce_pairs(dtype, op, hop)) ? 16 : 8;
 }
 // The fused RMSNorm kernel keeps all W values of a lane in registers and so
 // narrows its vectors to 4 bytes above 16 ranks.
@@ -126,12 +132,10 @@ constexpr int reduce_blocks_per_sm(int wcap, int u) { return (wcap <= 8 && wcap 
 // 13 to 16 ranks fold in batches of 8 (as above 16 ranks), which frees the
 // registers that 16 live vectors and 16 pointers take; measured on GB300 at
 // W = 16 (TB/s, plain -> batched): fp32 ring 5.4 -> 6.2, fp32 tree 6.3 -> 6.5,
-// bf16 tree 4.8 -> 6.4, int32 tree 5.8 -> 6.0, rings otherwise within 2 %.
-// At W = 12 the second batch is half empty and the plain fold stays ahead,
-// and per-hop bf16 sum / avg keeps the plain fold's packed bf16x2 pairs.
-constexpr bool reduce_batched16(int dtype, int op, bool hop) {
-    return !(dtype == MR_BF16 && hop && (op == MR_SUM || op == MR_AVG));
-}
+// bf16 tree 4.8 -> 6.4, int32 tree 5.8 -> 6.0, per-hop bf16 avg tree 6.0 ->
+// 6.4, rings otherwise within 2 %.  At W = 12 the second batch is half empty
+// and the plain fold stays ahead.
+constexpr int kBatchFromRanks = 13;
 
 // ---------------------------------------------------------------------------
 // Programmatic dependent launch.  Every kernel of the library is launched with

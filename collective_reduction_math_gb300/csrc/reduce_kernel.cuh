@@ -388,12 +388,53 @@ reduce_kernel(const __grid_constant__ ReduceParams P) {
     const bool rs = (P.mode == MODE_REDUCE_SCATTER);
     constexpr bool hop = DT == MR_BF16 && HOP;
     // per-hop bf16 sum / avg: fold two lanes per packed word (Bf16PairSum)
-    constexpr bool kPairs = hop && (OP == MR_SUM || OP == MR_AVG) && VB == 16;
+    constexpr bool kPairs = DT == MR_BF16 && HOP && (OP == MR_SUM || OP == MR_AVG);   // reduce_pairs()
     const uint64_t gmask = P.gmask;
     // a contribution as read: widened, pre-scaled, and for per-hop bf16 rounded
     auto contrib = [&](raw_t x) -> acc_t {
         const acc_t y = A::read(x, s);
         return (OP == MR_AVG && hop) ? A::hop(y) : y;
+    };
+
+    // Per-hop pairs: one 32-bit word holds two bf16 contributions as read
+    // (avg: pre-scaled in fp32, both lanes rounded to bf16 in one packed
+    // conversion, lo lane in x).
+    auto pair = [&](uint32_t w) -> uint32_t {
+        if constexpr (OP == MR_AVG) {
+            const float lo = __fmul_rn(__uint_as_float(w << 16), s);
+            const float hi = __fmul_rn(__uint_as_float(w & 0xFFFF0000u), s);
+            const __nv_bfloat162 p = __floats2bfloat162_rn(lo, hi);
+            uint32_t o;
+            memcpy(&o, &p, 4);
+            return o;
+        } else {
+            return w;
+        }
+    };
+    // The batched folds run on "units": a lane's fp32 (or int32) value, or
+    // with per-hop pairs a packed word of two bf16 lanes.
+    using unit_t = typename std::conditional<kPairs, uint32_t, acc_t>::type;
+    constexpr int UNITS = kPairs ? VB / 4 : LANES;
+    auto unit = [&](const Vec<VB>& v, int u) -> unit_t {
+        if constexpr (kPairs) return pair(v.w[u]);
+        else return contrib(get_lane<raw_t, VB>(v, u));
+    };
+    auto ucomb = [&](unit_t a, unit_t b) -> unit_t {
+        if constexpr (kPairs) return Bf16PairSum::combine(a, b);
+        else return comb<A>(a, b, hop);
+    };
+    auto utop = [&](unit_t (&y)[8], int Wb) -> unit_t {
+        if constexpr (kPairs) return tree_batch_top<Bf16PairSum>(y, Wb, false);
+        else return tree_batch_top<A>(y, Wb, hop);
+    };
+    auto upost = [&](const unit_t (&r)[UNITS], Vec<VB>& res) {
+        if constexpr (kPairs) {
+#pragma unroll
+            for (int u = 0; u < UNITS; ++u) res.w[u] = r[u];
+        } else {
+#pragma unroll
+            for (int l = 0; l < LANES; ++l) set_lane<raw_t, VB>(res, l, A::post(r[l], W));
+        }
     };
 
     // Input pointers in the current segment's accumulation order: in
@@ -468,7 +509,7 @@ reduce_kernel(const __grid_constant__ ReduceParams P) {
                 static_assert(U == 1, "the batched folds take one vector per thread per tile");
                 if (v0 < vb) {
                     const uint64_t off = v0 * VB;
-                    acc_t part[LANES], total[LANES];
+                    unit_t part[UNITS], total[UNITS];
                     bool have_total = false;
                     for (int b0 = 0; b0 < W; b0 += 8) {
                         Vec<VB> raw[8];
@@ -481,32 +522,30 @@ reduce_kernel(const __grid_constant__ ReduceParams P) {
                             if (p >= W) break;
                             if (p == 0) {
 #pragma unroll
-                                for (int l = 0; l < LANES; ++l) part[l] = contrib(get_lane<raw_t, VB>(raw[i], l));
+                                for (int u = 0; u < UNITS; ++u) part[u] = unit(raw[i], u);
                             } else if (ALGO == MR_HIER && ((gmask >> p) & 1u)) {
                                 if (have_total) {
 #pragma unroll
-                                    for (int l = 0; l < LANES; ++l) total[l] = comb<A>(total[l], part[l], hop);
+                                    for (int u = 0; u < UNITS; ++u) total[u] = ucomb(total[u], part[u]);
                                 } else {
 #pragma unroll
-                                    for (int l = 0; l < LANES; ++l) total[l] = part[l];
+                                    for (int u = 0; u < UNITS; ++u) total[u] = part[u];
                                 }
                                 have_total = true;
 #pragma unroll
-                                for (int l = 0; l < LANES; ++l) part[l] = contrib(get_lane<raw_t, VB>(raw[i], l));
+                                for (int u = 0; u < UNITS; ++u) part[u] = unit(raw[i], u);
                             } else {
 #pragma unroll
-                                for (int l = 0; l < LANES; ++l)
-                                    part[l] = comb<A>(part[l], contrib(get_lane<raw_t, VB>(raw[i], l)), hop);
+                                for (int u = 0; u < UNITS; ++u) part[u] = ucomb(part[u], unit(raw[i], u));
                             }
                         }
                     }
                     if (have_total) {
 #pragma unroll
-                        for (int l = 0; l < LANES; ++l) part[l] = comb<A>(total[l], part[l], hop);
+                        for (int u = 0; u < UNITS; ++u) part[u] = ucomb(total[u], part[u]);
                     }
                     Vec<VB> res;
-#pragma unroll
-                    for (int l = 0; l < LANES; ++l) set_lane<raw_t, VB>(res, l, A::post(part[l], W));
+                    upost(part, res);
                     if (rs) {
                         store_vec<VB>(static_cast<char*>(P.out[sg.k]) + off - sg.out_lo * EB, res);
                     } else {
@@ -533,7 +572,7 @@ reduce_kernel(const __grid_constant__ ReduceParams P) {
                 if (v0 < vb) {
                     const uint64_t off = v0 * VB;
                     const int M = (W + 7) >> 3;
-                    acc_t head[NB][LANES], top[NB][LANES];
+                    unit_t head[NB][UNITS], top[NB][UNITS];
 #pragma unroll
                     for (int m = 0; m < NB; ++m) {
                         if (m < M) {
@@ -543,13 +582,13 @@ reduce_kernel(const __grid_constant__ ReduceParams P) {
                             for (int q = 0; q < 8; ++q)
                                 if (q < Wb) raw[q] = load_vec<VB>(input(8 * m + q) + off);
 #pragma unroll
-                            for (int l = 0; l < LANES; ++l) {
-                                acc_t y[8];
+                            for (int u = 0; u < UNITS; ++u) {
+                                unit_t y[8];
 #pragma unroll
                                 for (int q = 0; q < 8; ++q)
-                                    if (q < Wb) y[q] = contrib(get_lane<raw_t, VB>(raw[q], l));
-                                head[m][l] = y[0];
-                                top[m][l] = tree_batch_top<A>(y, Wb, hop);
+                                    if (q < Wb) y[q] = unit(raw[q], u);
+                                head[m][u] = y[0];
+                                top[m][u] = utop(y, Wb);
                             }
                         }
                     }
@@ -559,36 +598,38 @@ reduce_kernel(const __grid_constant__ ReduceParams P) {
                         for (int m = B; m < NB; m += 2 * B) {
                             if (m < M) {
 #pragma unroll
-                                for (int l = 0; l < LANES; ++l) {
-                                    acc_t a = comb<A>(head[m][l], B == 1 ? top[m - 1][l] : head[m - B / 2][l], hop);
+                                for (int u = 0; u < UNITS; ++u) {
+                                    unit_t a = ucomb(head[m][u], B == 1 ? top[m - 1][u] : head[m - B / 2][u]);
                                     bool taken = false;
 #pragma unroll
                                     for (int h = B / 2; h >= 1; h >>= 1) {
                                         if (!taken && m + h < M) {
-                                            a = comb<A>(a, head[m + h][l], hop);
+                                            a = ucomb(a, head[m + h][u]);
                                             taken = true;
                                         }
                                     }
-                                    if (!taken && 8 * m + 1 < W) a = comb<A>(a, top[m][l], hop);
-                                    head[m][l] = a;
+                                    if (!taken && 8 * m + 1 < W) a = ucomb(a, top[m][u]);
+                                    head[m][u] = a;
                                 }
                             }
                         }
                     }
-                    Vec<VB> res;
+                    unit_t root[UNITS];
 #pragma unroll
-                    for (int l = 0; l < LANES; ++l) {
-                        acc_t a = head[0][l];
+                    for (int u = 0; u < UNITS; ++u) {
+                        unit_t a = head[0][u];
                         bool taken = false;
 #pragma unroll
                         for (int h = NB / 2; h >= 1; h >>= 1) {
                             if (!taken && h < M) {
-                                a = comb<A>(a, head[h][l], hop);
+                                a = ucomb(a, head[h][u]);
                                 taken = true;
                             }
                         }
-                        set_lane<raw_t, VB>(res, l, A::post(a, W));
+                        root[u] = a;
                     }
+                    Vec<VB> res;
+                    upost(root, res);
                     if (rs) {
                         store_vec<VB>(static_cast<char*>(P.out[sg.k]) + off - sg.out_lo * EB, res);
                     } else {
@@ -598,60 +639,46 @@ reduce_kernel(const __grid_constant__ ReduceParams P) {
                 }
                 continue;
             }
-            // U*W independent 16-byte loads in flight before the first fold.
-            Vec<VB> raw[U][WCAP];
+            if constexpr (!BATCH) {
+                // U*W independent 16-byte loads in flight before the first fold.
+                Vec<VB> raw[U][WCAP];
 #pragma unroll
-            for (int u = 0; u < U; ++u) {
-                const uint64_t v = v0 + (uint64_t)u * kThreads;
-                if (v < vb) {
-#pragma unroll
-                    for (int i = 0; i < WCAP; ++i)
-                        if (i < W) raw[u][i] = load_vec<VB>(input(i) + v * VB);
-                }
-            }
-#pragma unroll
-            for (int u = 0; u < U; ++u) {
-                const uint64_t v = v0 + (uint64_t)u * kThreads;
-                if (v >= vb) break;
-                const uint64_t off = v * VB;
-                Vec<VB> res;
-                if constexpr (kPairs) {
-                    // each word: two bf16 contributions, as read (avg:
-                    // pre-scaled in fp32 and rounded to bf16 per lane)
-                    auto pair = [&](uint32_t w) -> uint32_t {
-                        if constexpr (OP == MR_AVG) {
-                            // widen, pre-scale in fp32, round both lanes to
-                            // bf16 in one packed conversion (lo lane in x)
-                            const float lo = __fmul_rn(__uint_as_float(w << 16), s);
-                            const float hi = __fmul_rn(__uint_as_float(w & 0xFFFF0000u), s);
-                            const __nv_bfloat162 p = __floats2bfloat162_rn(lo, hi);
-                            uint32_t o;
-                            memcpy(&o, &p, 4);
-                            return o;
-                        } else {
-                            return w;
-                        }
-                    };
-#pragma unroll
-                    for (int k = 0; k < VB / 4; ++k) {
-                        uint32_t y[WCAP];
+                for (int u = 0; u < U; ++u) {
+                    const uint64_t v = v0 + (uint64_t)u * kThreads;
+                    if (v < vb) {
 #pragma unroll
                         for (int i = 0; i < WCAP; ++i)
-                            if (i < W) y[i] = pair(raw[u][i].w[k]);
-                        res.w[k] = fold<Bf16PairSum, ALGO, WCAP>(y, W, false, gmask);
+                            if (i < W) raw[u][i] = load_vec<VB>(input(i) + v * VB);
                     }
-                } else {
-                    acc_t r[LANES];
-                    fold_lanes<A, ALGO, WCAP, VB, LANES>(raw[u], W, gmask, hop, contrib, r);
-#pragma unroll
-                    for (int l = 0; l < LANES; ++l) set_lane<raw_t, VB>(res, l, A::post(r[l], W));
                 }
-                if (rs) {
-                    store_vec<VB>(static_cast<char*>(P.out[sg.k]) + off - sg.out_lo * EB, res);
-                } else {
 #pragma unroll
-                    for (int j = 0; j < WCAP; ++j)
-                        if (j < W) store_vec<VB>(static_cast<char*>(P.out[j]) + off, res);
+                for (int u = 0; u < U; ++u) {
+                    const uint64_t v = v0 + (uint64_t)u * kThreads;
+                    if (v >= vb) break;
+                    const uint64_t off = v * VB;
+                    Vec<VB> res;
+                    if constexpr (kPairs) {
+#pragma unroll
+                        for (int k = 0; k < VB / 4; ++k) {
+                            uint32_t y[WCAP];
+#pragma unroll
+                            for (int i = 0; i < WCAP; ++i)
+                                if (i < W) y[i] = pair(raw[u][i].w[k]);
+                            res.w[k] = fold<Bf16PairSum, ALGO, WCAP>(y, W, false, gmask);
+                        }
+                    } else {
+                        acc_t r[LANES];
+                        fold_lanes<A, ALGO, WCAP, VB, LANES>(raw[u], W, gmask, hop, contrib, r);
+#pragma unroll
+                        for (int l = 0; l < LANES; ++l) set_lane<raw_t, VB>(res, l, A::post(r[l], W));
+                    }
+                    if (rs) {
+                        store_vec<VB>(static_cast<char*>(P.out[sg.k]) + off - sg.out_lo * EB, res);
+                    } else {
+#pragma unroll
+                        for (int j = 0; j < WCAP; ++j)
+                            if (j < W) store_vec<VB>(static_cast<char*>(P.out[j]) + off, res);
+                    }
                 }
             }
         }
@@ -694,13 +721,11 @@ cudaError_t launch_reduce(const ReduceParams& P, int op, dim3 grid, cudaStream_t
                 if (rs) return launch_kernel(reduce_kernel<DT, OP, ALGO, 8, 16, reduce_unroll_for(8, true), HOP, false>, grid, 0, stream, 0, P);
                 return launch_kernel(reduce_kernel<DT, OP, ALGO, 8, 16, reduce_unroll_for(8, false), HOP, false>, grid, 0, stream, 0, P);
             case 16:
-                if constexpr (reduce_batched16(DT, OP, HOP)) {
-                    if (P.W > 12)
-                        return launch_kernel(reduce_kernel<DT, OP, ALGO, 16, 16, 1, HOP, true>, grid, 0, stream, 0, P);
-                }
+                if (P.W >= kBatchFromRanks)
+                    return launch_kernel(reduce_kernel<DT, OP, ALGO, 16, 16, 1, HOP, true>, grid, 0, stream, 0, P);
                 return launch_kernel(reduce_kernel<DT, OP, ALGO, 16, 16, reduce_unroll_for(16, false), HOP, false>, grid, 0, stream, 0, P);
             default:
-                return launch_kernel(reduce_kernel<DT, OP, ALGO, 64, reduce_vector_bytes(64, ALGO, Elem<DT>::kBytes),
+                return launch_kernel(reduce_kernel<DT, OP, ALGO, 64, reduce_vector_bytes(64, ALGO, DT, OP, HOP),
                                                    reduce_unroll_for(64, false), HOP, true>,
                                      grid, 0, stream, 0, P);
         }
