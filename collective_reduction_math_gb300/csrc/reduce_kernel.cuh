@@ -295,20 +295,21 @@ template <class raw_t, int VB> __device__ __forceinline__ void set_lane(Vec<VB>&
 }
 
 // The vector path's fold: all LANES elements of one vector at once.  The
-// hierarchical order, and the ring on bf16 (8-lane) and int32 vectors, run
-// positions outer and lanes inner, so each position's (warp-uniform)
-// decisions -- inside W, start of a group, per-hop rounding -- are taken once
-// per vector rather than once per lane; the tree, and the ring on fp32
-// vectors, run lane by lane.  Both choices were measured on GB300 (fp32 ring
-// sum faster lane by lane; int32 ring max at W = 16 6.0 against 4.8 TB/s
-// lanes inner).  contrib(x) widens, pre-scales and (per-hop) rounds one raw
+// hierarchical order, and the ring on bf16 (8-lane) and int32 vectors and on
+// fp32 vectors beyond 8 ranks, run positions outer and lanes inner, so each
+// position's (warp-uniform) decisions -- inside W, start of a group, per-hop
+// rounding -- are taken once per vector rather than once per lane; the tree,
+// and the ring on fp32 vectors up to 8 ranks, run lane by lane.  Each choice
+// was measured on GB300 (fp32 ring at W = 8 faster lane by lane; lanes inner:
+// int32 ring max at W = 16 6.0 against 4.8 TB/s, fp32 ring at W = 10-12 6.1
+// against 4.9).  contrib(x) widens, pre-scales and (per-hop) rounds one raw
 // contribution.
 template <class A, int ALGO, int WCAP, int VB, int LANES, class Contrib>
 __device__ __forceinline__ void fold_lanes(const Vec<VB> (&raw)[WCAP], int W, uint64_t gmask, bool hop,
                                            Contrib contrib, typename A::acc_t (&out)[LANES]) {
     using acc_t = typename A::acc_t;
     using raw_t = typename A::raw_t;
-    if constexpr (ALGO == MR_TREE || (ALGO == MR_RING && LANES <= 4 && std::is_same<acc_t, float>::value)) {
+    if constexpr (ALGO == MR_TREE || (ALGO == MR_RING && LANES <= 4 && std::is_same<acc_t, float>::value && WCAP <= 8)) {
 #pragma unroll
         for (int l = 0; l < LANES; ++l) {
             acc_t y[WCAP];
