@@ -56,14 +56,15 @@ allreduce_rmsnorm_kernel(const __grid_constant__ NormParams P) {
     const uint64_t H = P.hidden;
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     cg::cluster_group cluster = cg::this_cluster();
-    const int C = P.csize;
+    const int C = P.csize;                  // a power of two: divide by shifting
+    const int lc = 31 - __clz(C);
     const int crank = (int)cluster.block_rank();
-    const uint64_t first_row = blockIdx.x / C, row_stride = gridDim.x / C;
+    const uint64_t first_row = blockIdx.x >> lc, row_stride = gridDim.x >> lc;
     // This CTA's columns: vectors [v_lo, v_hi) (vector path) or elements
     // [c_lo, c_hi) (element path).
     const uint64_t nv_all = H / LANES;
-    const uint64_t v_lo = nv_all * crank / C, v_hi = nv_all * (crank + 1) / C;
-    const uint64_t c_lo = H * crank / C, c_hi = H * (crank + 1) / C;
+    const uint64_t v_lo = (nv_all * crank) >> lc, v_hi = (nv_all * (crank + 1)) >> lc;
+    const uint64_t c_lo = (H * crank) >> lc, c_hi = (H * (crank + 1)) >> lc;
 
     auto input = [&](const Segment& sg, int i) -> const char* {
         return static_cast<const char*>(P.in[order_rank<ALGO>(W, sg, i)]);
