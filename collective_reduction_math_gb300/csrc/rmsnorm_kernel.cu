@@ -74,6 +74,19 @@ allreduce_rmsnorm_kernel(const __grid_constant__ NormParams P) {
         while (e >= P.seg[s].hi) ++s;
         return s;
     };
+    // The segment holding element e, from an fp32 estimate of its chunk
+    // (floor(e * W / N), exact to within a chunk or two) and a short walk:
+    // a walk from segment 0 chains one parameter-bank load per segment
+    // passed, in front of the row's first load.
+    const uint64_t n_all = P.rows * H;
+    const float chunks_per_elem = (float)W / (float)n_all;
+    auto segment_near = [&](uint64_t e) {
+        int s = (int)((float)e * chunks_per_elem);
+        s = s < 0 ? 0 : s >= P.nseg ? P.nseg - 1 : s;
+        while (s > 0 && e < P.seg[s].lo) --s;
+        while (e >= P.seg[s].hi) ++s;
+        return s;
+    };
     // One element of pass 1: returns h and writes residual_out.
     auto element_h = [&](uint64_t e, int sgi) -> float {
         const Segment& sg = P.seg[sgi];
@@ -94,7 +107,7 @@ allreduce_rmsnorm_kernel(const __grid_constant__ NormParams P) {
     int parity = 0;
     for (uint64_t row = first_row; row < P.rows; row += row_stride, parity ^= 1) {
         const uint64_t base = row * H;
-        int sgi = segment_at(base + (P.vec ? v_lo * LANES : c_lo), 0);
+        int sgi = segment_near(base + (P.vec ? v_lo * LANES : c_lo));
         float ss = 0.0f;
 
         // ---- pass 1 -------------------------------------------------------
@@ -168,10 +181,13 @@ allreduce_rmsnorm_kernel(const __grid_constant__ NormParams P) {
             // cluster barrier per row keeps a fast CTA from overwriting a slot
             // a peer is still reading.
             cluster.sync();
-            if (threadIdx.x == 0) {
+            if (warp == 0) {
+                // lane r reads CTA r's total (one round of remote reads), then
+                // lane 0 adds them in rank order
+                const float mine = lane < C ? *cluster.map_shared_rank(&slice_total[parity], lane) : 0.0f;
                 float t = 0.0f;
-                for (int r = 0; r < C; ++r) t = __fadd_rn(t, *cluster.map_shared_rank(&slice_total[parity], r));
-                inv_shared = __fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(__fdiv_rn(t, (float)H), P.eps)));
+                for (int r = 0; r < C; ++r) t = __fadd_rn(t, __shfl_sync(0xffffffffu, mine, r));
+                if (lane == 0) inv_shared = __fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(__fdiv_rn(t, (float)H), P.eps)));
             }
         }
         __syncthreads();
