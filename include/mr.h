@@ -54,6 +54,8 @@
  *     stream order holds exactly as for a plain launch (also under CUDA graph
  *     capture).  Setting MR_PDL=0 in the environment before the first call
  *     launches every kernel in plain stream order instead.
+ *   - MR_DEBUG=1 in the environment logs each call's plan (the order MR_AUTO
+ *     chose, segments, grid) to stderr.
  *   - Errors in arguments return at once and launch nothing; a failed launch
  *     returns MR_ERR_CUDA.  mr_last_error() then describes the failure.
  *   - Allowed aliasing (in place) is listed per call; any other overlap between
