@@ -134,7 +134,9 @@ constexpr int reduce_blocks_per_sm(int wcap, int u) { return (wcap <= 8 && wcap 
 // W = 16 (TB/s, plain -> batched): fp32 ring 5.4 -> 6.2, fp32 tree 6.3 -> 6.5,
 // bf16 tree 4.8 -> 6.4, int32 tree 5.8 -> 6.0, per-hop bf16 avg tree 6.0 ->
 // 6.4, rings otherwise within 2 %.  At W = 12 the second batch is half empty
-// and the plain fold stays ahead.
+// and the plain fold stays ahead, except for the bf16 tree, whose plain fold
+// spills there (W = 10 / 12 bf16 tree avg 4.1 -> 5.1 / 4.6 -> 5.6 TB/s
+// batched): it folds in batches from 9 ranks.
 constexpr int kBatchFromRanks = 13;
 
 // ---------------------------------------------------------------------------

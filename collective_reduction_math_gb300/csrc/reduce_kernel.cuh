@@ -722,7 +722,7 @@ cudaError_t launch_reduce(const ReduceParams& P, int op, dim3 grid, cudaStream_t
                 if (rs) return launch_kernel(reduce_kernel<DT, OP, ALGO, 8, 16, reduce_unroll_for(8, true), HOP, false>, grid, 0, stream, 0, P);
                 return launch_kernel(reduce_kernel<DT, OP, ALGO, 8, 16, reduce_unroll_for(8, false), HOP, false>, grid, 0, stream, 0, P);
             case 16:
-                if (P.W >= kBatchFromRanks)
+                if (P.W >= kBatchFromRanks || (DT == MR_BF16 && ALGO == MR_TREE))
                     return launch_kernel(reduce_kernel<DT, OP, ALGO, 16, 16, 1, HOP, true>, grid, 0, stream, 0, P);
                 return launch_kernel(reduce_kernel<DT, OP, ALGO, 16, 16, reduce_unroll_for(16, false), HOP, false>, grid, 0, stream, 0, P);
             default:
