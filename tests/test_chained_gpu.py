@@ -197,3 +197,70 @@ def test_pdl_off_gives_the_same_results():
     env = dict(os.environ, MR_PDL="0")
     p = subprocess.run([sys.executable, "-c", code], env=env, capture_output=True, text=True, timeout=300)
     assert p.returncode == 0 and p.stdout.strip().endswith("ok"), p.stdout + p.stderr
+
+
+@pytest.mark.parametrize("rows", [64, 600])
+def test_rmsnorm_replayed_from_a_graph_matches_eager(mr, rows):
+    """The fused RMSNorm (a thread-block-cluster launch for few rows) captured
+    into a CUDA graph and replayed twice gives exactly the eager call's
+    outputs; the eager call is held to the oracle by test_rmsnorm_gpu."""
+    import torch
+    W, H = 8, 8192
+    N = rows * H
+    xs = [to_device(h, "bf16") for h in synth.random_values(31, W, N, "bf16")]
+    res = to_device(synth.random_values(32, 1, N, "bf16")[0], "bf16")
+    wt = to_device(synth.random_values(33, 1, H, "bf16")[0], "bf16")
+    eager = [torch.empty_like(x) for x in xs]
+    eager_res = torch.empty_like(res)
+    mr.mr_allreduce_rmsnorm(xs, eager, wt, residual=res, residual_out=eager_res, eps=1e-6)
+    ys = [torch.empty_like(x) for x in xs]
+    rout = torch.empty_like(res)
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(side):
+        with torch.cuda.graph(graph, stream=side):
+            mr.mr_allreduce_rmsnorm(xs, ys, wt, residual=res, residual_out=rout, eps=1e-6)
+    torch.cuda.current_stream().wait_stream(side)
+    for _ in range(2):
+        for y in ys:
+            y.zero_()
+        graph.replay()
+        torch.cuda.synchronize()
+        assert torch.equal(rout, eager_res)
+        for y, e in zip(ys, eager):
+            assert torch.equal(y, e)
+
+
+def test_sign_ef_steps_replayed_from_a_graph_match_eager(mr):
+    """Two sign-compressed reduce-scatter steps (two kernels each, the second
+    reading the first's partials) replayed from a CUDA graph give exactly two
+    eager steps: outputs, scales and the carried residual."""
+    import torch
+    W, N = 8, 8 * 30000
+    g = [torch.from_numpy(x).cuda() for x in synth.normal(41, W, N, 1e-3, "fp32")]
+    e0 = synth.normal(42, W, N, 1e-4, "fp32")
+    e_eager = [torch.from_numpy(x).cuda() for x in e0]
+    e_graph = [torch.from_numpy(x).cuda() for x in e0]
+    C = N // W
+    out_e = [torch.empty(C, device="cuda") for _ in range(W)]
+    out_g = [torch.empty(C, device="cuda") for _ in range(W)]
+    s_e, s_g = torch.empty(W, device="cuda"), torch.empty(W, device="cuda")
+    ws_e = torch.empty(mr.mr_sign_ef_workspace_bytes(W, N), dtype=torch.uint8, device="cuda")
+    ws_g = torch.empty_like(ws_e)
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(side):
+        with torch.cuda.graph(graph, stream=side):
+            mr.mr_reduce_scatter_sign_ef(g, e_graph, out_g, scales=s_g, workspace=ws_g, op="avg", algo="ring")
+    torch.cuda.current_stream().wait_stream(side)
+    torch.cuda.synchronize()
+    for step in range(2):
+        mr.mr_reduce_scatter_sign_ef(g, e_eager, out_e, scales=s_e, workspace=ws_e, op="avg", algo="ring")
+        graph.replay()
+        torch.cuda.synchronize()
+        assert torch.equal(s_e, s_g), f"step {step}: scales"
+        for k in range(W):
+            assert torch.equal(out_e[k], out_g[k]), f"step {step}: shard {k}"
+            assert torch.equal(e_eager[k], e_graph[k]), f"step {step}: residual {k}"
