@@ -400,11 +400,15 @@ mr_status_t mr_all_gather(const void* const* send, void* const* recv, int W, siz
     P.W = W;
     P.C = C;
     P.esize = (int)b;
-    bool vec = (C * b) % 16 == 0;
-    for (int r = 0; r < W; ++r) vec = vec && ((uintptr_t)send[r] % 16 == 0) && ((uintptr_t)recv[r] % 16 == 0);
-    P.vec = vec ? 1 : 0;
-    const uint64_t per_tile = vec ? (uint64_t)mr::kThreads * mr::kGatherUnroll : (uint64_t)mr::kThreads;
-    const uint64_t units = vec ? (C * b) / 16 : C;
+    auto aligned = [&](size_t a) {
+        bool ok = (C * b) % a == 0;
+        for (int r = 0; r < W; ++r) ok = ok && ((uintptr_t)send[r] % a == 0) && ((uintptr_t)recv[r] % a == 0);
+        return ok;
+    };
+    P.vec = aligned(32) ? 2 : aligned(16) ? 1 : 0;
+    const int vb = P.vec == 2 ? 32 : 16;
+    const uint64_t per_tile = P.vec ? (uint64_t)mr::kThreads * (mr::kGatherBytesPerThread / vb) : (uint64_t)mr::kThreads;
+    const uint64_t units = P.vec ? (C * b) / vb : C;
     const uint64_t tiles = std::max<uint64_t>(1, (units + per_tile - 1) / per_tile) * (uint64_t)W;
     const uint64_t gx = std::min<uint64_t>((uint64_t)sm_count() * mr::kGatherBlocksPerSm, tiles);
     const dim3 grid((unsigned)gx, 1, 1);

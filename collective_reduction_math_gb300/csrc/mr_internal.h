@@ -12,7 +12,7 @@ namespace mr {
 constexpr int kMaxRanks = MR_MAX_RANKS;
 constexpr int kMaxSegments = 2 * MR_MAX_RANKS + 2;
 constexpr int kThreads = 256;       // threads per CTA for every kernel
-constexpr int kGatherUnroll = 8;        // 16-byte vectors per thread per all-gather tile
+constexpr int kGatherBytesPerThread = 128;   // bytes each thread loads per all-gather tile
 constexpr int kGatherBlocksPerSm = 16;  // all-gather CTAs per SM in the grid (several waves)
 
 // A run of elements with one accumulation order and one output placement:
@@ -99,7 +99,8 @@ struct GatherParams {
     uint64_t C;     // elements per shard
     int W;
     int esize;      // bytes per element (2 or 4)
-    int vec;        // 1: 16-byte vector path (pointers aligned, C*esize % 16 == 0)
+    int vec;        // 2: 32-byte vectors, 1: 16-byte vectors (every pointer and
+                    // C*esize aligned to the width), 0: element by element
 };
 
 // The reduce kernel variant for a given W: register slots for W contributions

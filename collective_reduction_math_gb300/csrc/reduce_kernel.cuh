@@ -187,7 +187,7 @@ __device__ __forceinline__ typename A::acc_t fold_tree(typename A::acc_t (&y)[WC
     return a;
 }
 
-// The in-batch part of the tree fold for more than 16 ranks.  Positions come
+// The in-batch part of the batched tree fold.  Positions come
 // in batches of 8, [8m, 8m+8); positions 8m+1 .. 8m+7 lie in whole subtrees
 // of the batch (the subtree of a node at level b spans (p-b, p+b)), so the
 // levels 2 and 4 of a batch fold on their own (y[0] is the batch head, at
@@ -439,9 +439,9 @@ reduce_kernel(const __grid_constant__ ReduceParams P) {
     };
 
     // Input pointers in the current segment's accumulation order: in
-    // registers for up to 16 ranks, in a shared-memory table beyond that.
-    // BATCH: the ranks are loaded and folded in batches of 8 (only 8 vectors
-    // live at a time), and the pointer table sits in shared memory.
+    // registers for the plain fold, in a shared-memory table for the batched
+    // one (BATCH: the ranks are loaded and folded in batches of 8, so only 8
+    // vectors are live at a time).
     constexpr bool kTable = BATCH;
     constexpr bool kBatched = BATCH && ALGO != MR_TREE;
     constexpr bool kTreeBatched = BATCH && ALGO == MR_TREE;
