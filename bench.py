@@ -482,7 +482,48 @@ def extras(mr, torch, dev):
     ut = back_to_back_us(unfused, 20)
     out["fused_vs_unfused_ddp_bucket"] = {"fused_us": ft, "rs_then_ag_us": ut,
                                           "fused_bytes": 2 * W * N * 4, "unfused_bytes": (2 * W + 2) * N * 4}
+    del xs, ys, sh, bufs
+    torch.cuda.empty_cache()
+    out["next_rows"] = next_rows(mr, torch, dev)
     return out
+
+
+# The rows beyond the hot path: (label, workload, collective, algo, group, per-hop).
+NEXT_ROWS = [
+    ("fused all-reduce + residual + RMSNorm, prefill", "tp_prefill_rmsnorm_bf16_w8", None, "ring", None, False),
+    ("fused all-reduce + residual + RMSNorm, decode", "tp_decode_rmsnorm_bf16_w8", None, "ring", None, False),
+    ("1-bit sign + error feedback, reduce-scatter", "sign_ef_fp32_w8", "reduce_scatter_sign_ef", "ring", None, False),
+    ("1-bit sign + error feedback, all-reduce", "sign_ef_fp32_w8", "allreduce_sign_ef", "ring", None, False),
+    ("hierarchical 2 x 8 all-reduce", "hier_bf16_w16", None, "hier", 8, False),
+    ("hierarchical 2 x 8 all-reduce, per-hop bf16", "hier_bf16_w16", None, "hier", 8, True),
+    ("ring all-reduce, per-hop bf16", "hier_bf16_w16", None, "ring", None, True),
+    ("FSDP reduce-scatter, per-hop bf16", "fsdp_bf16_w8", "reduce_scatter", "ring", None, True),
+]
+
+
+def next_rows(mr, torch, dev):
+    """One line per row beyond the hot path: its workload as bench.py runs it
+    with --workload (default op), timed back to back (as CUDA graphs of
+    GRAPH_STEPS steps below GRAPH_BELOW_BYTES), in GB/s of its algorithmic
+    bytes and as a fraction of the measured HBM peak."""
+    peak, _ = peaks()
+    rows = []
+    for label, workload, collective, algo, group, hop in NEXT_ROWS:
+        args = argparse.Namespace(workload=workload, collective=collective, op=None, algo=algo, group=group,
+                                  per_hop=hop, n=None)
+        S = Step(args, mr, torch, dev)
+        for _ in range(3):
+            S.call()
+        small = S.bytes < GRAPH_BELOW_BYTES
+        t = graph_us(S.call, GRAPH_STEPS) if small else back_to_back_us(S.call, 50)
+        gbs = S.bytes / (t * 1e-6) / 1e9
+        rows.append({"row": label, "workload": workload, "collective": S.collective, "op": S.op, "algo": algo,
+                     "group": group, "per_hop_rounding": hop, "us_per_step": t, "bytes_per_step": S.bytes,
+                     "gbs": gbs, "frac_of_hbm_peak": gbs / peak,
+                     "timing": f"CUDA graph of {GRAPH_STEPS} steps" if small else "50 steps back to back"})
+        del S
+        torch.cuda.empty_cache()
+    return rows
 
 
 class Step:
