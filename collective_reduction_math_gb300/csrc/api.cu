@@ -545,7 +545,15 @@ mr_status_t mr_allreduce_rmsnorm(const void* const* send, void* const* recv, int
     P.csize = csize;
     const size_t slice = (hidden + csize - 1) / csize + lanes;
     const size_t smem = ((slice * 4 + 15) / 16) * 16;
-    const size_t per_sm = std::max<size_t>(1, std::min<size_t>(8, (200 * 1024) / (smem + 1024)));
+    // One whole wave of resident CTAs, looping over the rows.  Residency is
+    // the smaller of what the kernel's register budget allows (3 per SM up to
+    // 8 ranks, 2 up to 16, else 1: its launch bounds) and what shared memory
+    // allows (227 KB per SM, the row slice plus about 1 KB per CTA).  A grid
+    // that left a partial last wave measured up to 10 % slower on GB300
+    // (W = 8 bf16, hidden 12288: 5032 against 5546 GB/s).
+    const size_t reg_resident = W <= 8 ? 3 : W <= 16 ? 2 : 1;
+    const size_t smem_resident = std::max<size_t>(1, (227 * 1024) / (smem + 1024));
+    const size_t per_sm = std::min(reg_resident, smem_resident);
     const size_t clusters = std::min<size_t>(rows, std::max<size_t>(1, sms * per_sm / csize));
     const dim3 grid((unsigned)(clusters * csize), 1, 1);
     const cudaError_t err = mr::launch_allreduce_rmsnorm(P, dtype, algo, grid, smem, (cudaStream_t)stream);
