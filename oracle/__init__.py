@@ -208,7 +208,8 @@ def allreduce_rmsnorm(dtype: str, algo: str, inputs, rows: int, hidden: int, wei
 
 
 def sign_ef_scales(grads, errs):
-    """s_r = ||g_r + e_r||_1 / N for every rank (fp32 values, fp64 sum)."""
+    """s_r = ||g_r + e_r||_1 / N for every rank: the exact sum of the fp32
+    magnitudes over the exact N, rounded once to the nearest fp32."""
     W, N = len(grads), grads[0].size
     _check_inputs("fp32", grads, N)
     _check_inputs("fp32", errs, N)

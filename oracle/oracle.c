@@ -459,17 +459,103 @@ int or_allreduce_rmsnorm(int dtype, int algo, int W, size_t rows, size_t hidden,
 
 /* p_r = g_r + e_r (one fp32 add per element), and the rank's scale
  *     s_r = ||p_r||_1 / N,
- * the L1 norm summed in fp64 over the whole buffer, divided in fp64 and
- * rounded once to fp32. */
+ * read as a real number: the exact sum of the |p| divided exactly by N, then
+ * rounded once to the nearest fp32, ties to even.  (A NaN among the p makes
+ * the scale NaN; otherwise an infinite |p| makes it +infinity.)
+ *
+ * Every finite fp32 is an integer multiple of 2^-149, the smallest subnormal,
+ * and below 2^277 of those units, so the sum is kept exactly as an integer
+ * count of 2^-149 units in L1_WORDS 32-bit words (384 bits: room for 2^107
+ * terms).  The quotient by N is taken bit by bit, from the top, like long
+ * division on paper. */
+#define L1_WORDS 12
+#define L1_BITS (32 * L1_WORDS)
+
+typedef struct {
+    uint32_t w[L1_WORDS];   /* little-endian words of the count of 2^-149 units */
+    int any_nan, any_inf;
+} l1_sum_t;
+
+static int big_bit(const uint32_t* w, int bit) { return (int)((w[bit / 32] >> (bit % 32)) & 1u); }
+
+/* sum += |a| */
+static void l1_add(l1_sum_t* s, float a) {
+    uint32_t u;
+    memcpy(&u, &a, 4);
+    u &= 0x7FFFFFFFu;
+    uint32_t biased = u >> 23, frac = u & 0x7FFFFFu;
+    if (biased == 255u) {
+        if (frac) s->any_nan = 1;
+        else s->any_inf = 1;
+        return;
+    }
+    /* |a| = m * 2^(pos - 149): a normal number carries the implicit bit and
+     * exponent biased - 150; a subnormal has exponent -149. */
+    uint64_t m = biased ? (uint64_t)(frac | 0x800000u) : (uint64_t)frac;
+    int pos = biased ? (int)biased - 1 : 0;
+    uint64_t v = m << (pos % 32);       /* below 2^55: spans two words */
+    uint64_t carry = 0;
+    for (int j = pos / 32; j < L1_WORDS; j++) {
+        uint64_t add = 0;
+        if (j == pos / 32) add = v & 0xFFFFFFFFu;
+        else if (j == pos / 32 + 1) add = v >> 32;
+        uint64_t t = (uint64_t)s->w[j] + add + carry;
+        s->w[j] = (uint32_t)t;
+        carry = t >> 32;
+    }
+}
+
+/* The nearest fp32 to S / N, ties to even, for S = the sum in 2^-149 units. */
+static float l1_mean(const l1_sum_t* s, uint64_t N) {
+    if (s->any_nan) return NAN;
+    if (s->any_inf) return INFINITY;
+    /* Q = floor(S / N), R = S mod N */
+    uint32_t q[L1_WORDS];
+    memset(q, 0, sizeof(q));
+    uint64_t r = 0;
+    for (int bit = L1_BITS - 1; bit >= 0; bit--) {
+        int top = (int)(r >> 63);
+        r = (r << 1) | (uint64_t)big_bit(s->w, bit);
+        if (top || r >= N) {            /* (top: the true value passed 2^64, so it exceeds N) */
+            r -= N;
+            q[bit / 32] |= 1u << (bit % 32);
+        }
+    }
+    int len = 0;                        /* bit length of Q */
+    for (int bit = L1_BITS - 1; bit >= 0; bit--)
+        if (big_bit(q, bit)) {
+            len = bit + 1;
+            break;
+        }
+    if (len <= 24) {
+        /* S / N < 2^-125: the fp32 values there (subnormals and the lowest
+         * normal binade) are the integer multiples of 2^-149, so round
+         * Q + R/N to an integer: up past one half, a tie to the even one. */
+        uint64_t m = (uint64_t)q[0];
+        if (r > N - r || (r == N - r && (m & 1u))) m++;
+        return (float)ldexp((double)m, -149);
+    }
+    /* keep the top 24 bits of Q; the rest of Q and R/N decide the rounding */
+    int shift = len - 24;
+    uint64_t m = 0;
+    for (int bit = len - 1; bit >= shift; bit--) m = (m << 1) | (uint64_t)big_bit(q, bit);
+    int half = big_bit(q, shift - 1);
+    int below = r != 0;
+    for (int bit = shift - 2; bit >= 0 && !below; bit--) below = big_bit(q, bit);
+    if (half && (below || (m & 1u))) m++;
+    return (float)ldexp((double)m, shift - 149);   /* exact, or +inf past the largest fp32 */
+}
+
 int or_sign_ef_scales(int W, size_t N, const float* const* grad, const float* const* err, float* scales) {
     if (W < 1 || W > OR_MAX_RANKS || N == 0) return -1;
     for (int r = 0; r < W; r++) {
-        double l1 = 0.0;
+        l1_sum_t sum;
+        memset(&sum, 0, sizeof(sum));
         for (size_t e = 0; e < N; e++) {
             float p = grad[r][e] + err[r][e];
-            l1 += fabs((double)p);
+            l1_add(&sum, p);
         }
-        scales[r] = (float)(l1 / (double)N);
+        scales[r] = l1_mean(&sum, (uint64_t)N);
     }
     return 0;
 }

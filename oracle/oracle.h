@@ -101,7 +101,9 @@ int or_allreduce_rmsnorm(int dtype, int algo, int W, size_t rows, size_t hidden,
                          void* const* out, void* residual_out);
 
 /* 1-bit sign compression with error feedback (fp32 only).
- * or_sign_ef_scales: s_r = ||g_r + e_r||_1 / N for every rank (fp64 sum).
+ * or_sign_ef_scales: s_r = ||g_r + e_r||_1 / N for every rank: the exact
+ *   sum of the magnitudes, divided exactly by N, rounded once to the nearest
+ *   fp32 (ties to even); NaN if any p is NaN, else +inf if any |p| is.
  * or_sign_ef_collective: with the given scales, decode q = sign(p) * s_r,
  * update err[r] = p - q in place, and reduce the q (sum or avg) into out:
  * mode 0 all-reduce (out[j]: N elements), mode 1 reduce-scatter (out[k]:
