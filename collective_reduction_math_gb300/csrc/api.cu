@@ -567,12 +567,17 @@ mr_status_t mr_allreduce_rmsnorm(const void* const* send, void* const* recv, int
 
 size_t mr_sign_ef_workspace_bytes(int W, size_t N) {
     if (W < 1 || W > MR_MAX_RANKS) return 0;
-    return (size_t)W * (size_t)mr::sign_blocks(N) * sizeof(double);
+    return (size_t)mr::sign_workspace_bytes(W, N);
 }
 
-static mr_status_t run_sign_ef(const char* what, int mode, const void* const* grad, void* const* err,
-                               void* const* recv, float* scales, int W, size_t N, mr_op_t op, mr_algo_t algo,
-                               void* workspace, size_t workspace_bytes, void* stream) {
+}  // extern "C"
+
+// The sign-compressed reductions.  `scratch`, when given, supplies the
+// workspace once every argument has been checked (the allocation-free entry
+// point); otherwise the caller's workspace is used.
+mr_status_t mr::run_sign_ef(const char* what, int mode, const void* const* grad, void* const* err,
+                            void* const* recv, float* scales, int W, size_t N, mr_op_t op, mr_algo_t algo,
+                            void* workspace, size_t workspace_bytes, void* stream, ScratchFn scratch) {
     g_last_error.clear();
     mr_status_t st = check_common(grad, recv, W, MR_FP32);
     if (st == MR_OK) st = check_op_algo(op, algo);
@@ -582,12 +587,14 @@ static mr_status_t run_sign_ef(const char* what, int mode, const void* const* gr
     if (mode == mr::MODE_REDUCE_SCATTER && N % (size_t)W != 0)
         return fail(MR_ERR_INVALID_ARGUMENT, "%s needs N (%zu) divisible by W (%d)", what, N, W);
     if (N == 0) return MR_OK;
+    if (N >= mr::kSignMaxN)
+        return fail(MR_ERR_INVALID_ARGUMENT, "%s takes N below 2^37 elements per rank (N = %zu)", what, N);
     if ((st = check_pointers(grad, recv, W, MR_FP32)) != MR_OK) return st;
     for (int r = 0; r < W; ++r)
         if (!err[r] || ((uintptr_t)err[r] & 3u)) return fail(MR_ERR_INVALID_ARGUMENT, "err[%d] is NULL or misaligned", r);
     if ((uintptr_t)scales & 3u) return fail(MR_ERR_INVALID_ARGUMENT, "scales is misaligned");
     const size_t need = mr_sign_ef_workspace_bytes(W, N);
-    if (!workspace || ((uintptr_t)workspace & 7u) || workspace_bytes < need)
+    if (!scratch && (!workspace || ((uintptr_t)workspace & 7u) || workspace_bytes < need))
         return fail(MR_ERR_INVALID_ARGUMENT, "workspace must be 8-byte aligned and hold %zu bytes", need);
 
     const size_t bytes = N * 4, C = N / (size_t)W, out_bytes = mode == mr::MODE_REDUCE_SCATTER ? C * 4 : bytes;
@@ -599,13 +606,22 @@ static mr_status_t run_sign_ef(const char* what, int mode, const void* const* gr
         rs[n++] = {(uintptr_t)err[r], (uintptr_t)err[r] + bytes, r, ERR};
     }
     if (scales) rs[n++] = {(uintptr_t)scales, (uintptr_t)scales + (size_t)W * 4, 0, SCALES};
-    rs[n++] = {(uintptr_t)workspace, (uintptr_t)workspace + need, 0, WORKSPACE};
+    if (!scratch) rs[n++] = {(uintptr_t)workspace, (uintptr_t)workspace + need, 0, WORKSPACE};
     st = check_overlaps(rs, n, [&](const Range& x, const Range& y) {
         if (!(x.kind == SEND && y.kind == RECV && x.rank == y.rank)) return false;
         if (mode == mr::MODE_REDUCE_SCATTER) return y.lo == x.lo + (size_t)x.rank * C * 4;
         return y.lo == x.lo;
     });
     if (st != MR_OK) return st;
+    if (scratch) {
+        // The library's own scratch (no caller buffer can overlap it).
+        const cudaError_t e = scratch(&workspace, &workspace_bytes);
+        if (e != cudaSuccess)
+            return fail(MR_ERR_CUDA, "%s: locating the static scratch failed: %s", what, cudaGetErrorString(e));
+        if (workspace_bytes < need)
+            return fail(MR_ERR_INVALID_ARGUMENT, "%s: the static scratch holds %zu bytes, the call needs %zu", what,
+                        workspace_bytes, need);
+    }
 
     if (algo == MR_AUTO) algo = resolve_auto(MR_FP32, W, N, mode == mr::MODE_REDUCE_SCATTER, nullptr);
     mr::SignParams P;
@@ -614,12 +630,12 @@ static mr_status_t run_sign_ef(const char* what, int mode, const void* const* gr
         P.err[r] = err[r];
         P.out[r] = recv[r];
     }
-    P.partials = static_cast<double*>(workspace);
+    P.partials = static_cast<uint32_t*>(workspace);
     P.scales = scales;
     P.N = N;
     P.W = W;
     P.mode = mode;
-    P.nb = mr::sign_blocks(N);
+    P.nb = mr::sign_blocks(W, N);
     P.avg = (float)(1.0 / (double)W);
     P.nseg = plan_segments(W, N, algo, P.seg);
     const int vb = mr::sign_vector_bytes(W);
@@ -660,17 +676,19 @@ static mr_status_t run_sign_ef(const char* what, int mode, const void* const* gr
     return MR_OK;
 }
 
+extern "C" {
+
 mr_status_t mr_allreduce_sign_ef(const void* const* grad, void* const* err, void* const* recv, float* scales,
                                  int W, size_t N, mr_op_t op, mr_algo_t algo, void* workspace,
                                  size_t workspace_bytes, void* stream) {
-    return run_sign_ef("allreduce_sign_ef", mr::MODE_ALLREDUCE, grad, err, recv, scales, W, N, op, algo, workspace,
+    return mr::run_sign_ef("allreduce_sign_ef", mr::MODE_ALLREDUCE, grad, err, recv, scales, W, N, op, algo, workspace,
                        workspace_bytes, stream);
 }
 
 mr_status_t mr_reduce_scatter_sign_ef(const void* const* grad, void* const* err, void* const* recv, float* scales,
                                       int W, size_t N, mr_op_t op, mr_algo_t algo, void* workspace,
                                       size_t workspace_bytes, void* stream) {
-    return run_sign_ef("reduce_scatter_sign_ef", mr::MODE_REDUCE_SCATTER, grad, err, recv, scales, W, N, op, algo,
+    return mr::run_sign_ef("reduce_scatter_sign_ef", mr::MODE_REDUCE_SCATTER, grad, err, recv, scales, W, N, op, algo,
                        workspace, workspace_bytes, stream);
 }
 

@@ -68,7 +68,7 @@ struct SignParams {
     const void* grad[kMaxRanks];
     void* err[kMaxRanks];       // read, then overwritten with the new residual
     void* out[kMaxRanks];
-    double* partials;           // workspace: W x nb per-block L1 partials
+    uint32_t* partials;         // workspace: per rank, kL1Words words x nb blocks (word-major)
     float* scales;              // W scales out (device)
     Segment seg[kMaxSegments];
     uint64_t tile_start[kMaxSegments + 1];
@@ -84,12 +84,29 @@ struct SignParams {
     float avg;                  // fl32(1/W)
 };
 
-// L1 blocks per rank for a buffer of N elements (the workspace holds W*nb doubles).
-constexpr uint64_t kSignMaxBlocks = 256;
-inline int sign_blocks(uint64_t N) {
+// Exact L1 sums.  The magnitude of a finite fp32 is an integer multiple of
+// 2^-149 (the smallest subnormal) below 2^277 of those units, so a sum of up
+// to 2^43 magnitudes is an integer below 2^320: ten 32-bit limbs.  A block's
+// partial is those ten limbs (carries propagated) and a flags word (bit 0: an
+// infinite |p| was seen, bit 1: a NaN).
+constexpr int kL1Limbs = 10;
+constexpr int kL1Words = kL1Limbs + 1;
+// The largest N the sign path takes: the scale's final division keeps the
+// sum's top 64 bits, and N below 2^37 leaves at least 26 quotient bits.
+constexpr uint64_t kSignMaxN = 1ull << 37;
+
+// L1 blocks per rank: one per 8192 elements, at most 2048 / W (so a call
+// never needs more than 2048 partials), at least one.
+inline int sign_blocks(int W, uint64_t N) {
+    const uint64_t cap = (uint64_t)(2048 / (W < 1 ? 1 : W));
     const uint64_t nb = (N + 8191) / 8192;
-    return (int)(nb < 1 ? 1 : nb > kSignMaxBlocks ? kSignMaxBlocks : nb);
+    return (int)(nb < 1 ? 1 : nb > cap ? cap : nb);
 }
+// Workspace of the sign path: the partials, in bytes.
+inline uint64_t sign_workspace_bytes(int W, uint64_t N) {
+    return (uint64_t)W * (uint64_t)kL1Words * (uint64_t)sign_blocks(W, N) * sizeof(uint32_t);
+}
+constexpr uint64_t kSignMaxWorkspaceBytes = 2048ull * kL1Words * sizeof(uint32_t);
 // Vector width of the decode-and-reduce kernel for a given W.
 constexpr int sign_vector_bytes(int W) { return W <= 8 ? 16 : W <= 16 ? 8 : 4; }
 
@@ -211,6 +228,11 @@ MR_DECLARE_REDUCE(int32, hier)
 cudaError_t launch_all_gather(const GatherParams& P, dim3 grid, cudaStream_t s);
 mr_status_t report_error(mr_status_t st, const char* fmt, ...);
 cudaError_t launch_sign_l1(const SignParams& P, cudaStream_t s);
+// Supplies a workspace (pointer and size) for the sign path.
+using ScratchFn = cudaError_t (*)(void** workspace, size_t* bytes);
+mr_status_t run_sign_ef(const char* what, int mode, const void* const* grad, void* const* err, void* const* recv,
+                        float* scales, int W, size_t N, mr_op_t op, mr_algo_t algo, void* workspace,
+                        size_t workspace_bytes, void* stream, ScratchFn scratch = nullptr);
 cudaError_t launch_sign_ef(const SignParams& P, int op, int algo, dim3 grid, cudaStream_t s);
 cudaError_t launch_allreduce_rmsnorm(const NormParams& P, int dtype, int algo, dim3 grid, size_t smem, cudaStream_t s);
 

@@ -11,36 +11,85 @@
 // the library itself (loaded with it, held by every GPU that loads the
 // library until the process exits), and hands its address to the existing
 // reduce-scatter entry point.
+#include <cuda.h>
 #include <cuda_runtime.h>
 
-#include <atomic>
+#include <mutex>
 
 #include "mr.h"
 #include "mr_internal.h"
 
 namespace {
 
-// The scratch: room for W * blocks fp64 partials.  64 KiB covers every N for
-// W <= 32 and, at W = 64, buffers of up to 2^20 elements per rank.
-constexpr size_t kScratchBytes = 64 * 1024;
-static __device__ __align__(256) double g_sign_scratch[kScratchBytes / sizeof(double)];
+// The scratch: 96 KiB.  A call never needs more than 2048 partials of
+// kL1Words 32-bit words (88 KiB), whatever W and N are.
+constexpr size_t kScratchBytes = 96 * 1024;
+static_assert(mr::kSignMaxWorkspaceBytes <= kScratchBytes, "the static scratch must hold every call's partials");
+static __device__ __align__(256) uint32_t g_sign_scratch[kScratchBytes / sizeof(uint32_t)];
 
+// The array's device address, per device, tagged with the CUDA context it
+// was looked up in.  Host code sees only a host-side stand-in under the
+// array's name, so the address is asked of the runtime with the device
+// current.  A device reset (cudaDeviceReset) destroys the context and the
+// module with it; the next call finds a new context id and looks the address
+// up again instead of using the old one.
 constexpr int kMaxDevices = 64;
-std::atomic<void*> g_scratch_addr[kMaxDevices];
+struct Cached {
+    unsigned long long ctx_id = 0;
+    void* addr = nullptr;
+};
+Cached g_cache[kMaxDevices];
+std::mutex g_cache_mutex;
 
-// The array's device address on the current device.  Host code sees only a
-// host-side stand-in under the array's name, so the address is asked of the
-// runtime, once per device, with that device current.
-cudaError_t scratch_address(void** out) {
+using CtxGetCurrent = CUresult (*)(CUcontext*);
+using CtxGetId = CUresult (*)(CUcontext, unsigned long long*);
+
+// The current context's unique id, through the driver entry points the
+// runtime hands out (no link to the driver library).  False when there is no
+// current context or the driver does not offer the calls.
+bool current_context_id(unsigned long long* id) {
+    static CtxGetCurrent get_current = nullptr;
+    static CtxGetId get_id = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void* f = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &f, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            get_current = reinterpret_cast<CtxGetCurrent>(f);
+        f = nullptr;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &f, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            get_id = reinterpret_cast<CtxGetId>(f);
+        cudaGetLastError();
+    });
+    if (!get_current || !get_id) return false;
+    CUcontext ctx = nullptr;
+    if (get_current(&ctx) != CUDA_SUCCESS || !ctx) return false;
+    return get_id(ctx, id) == CUDA_SUCCESS;
+}
+
+cudaError_t scratch_address(void** out, size_t* bytes) {
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
     if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
-    void* p = g_scratch_addr[dev].load(std::memory_order_acquire);
-    if (!p) {
-        e = cudaGetSymbolAddress(&p, g_sign_scratch);
-        if (e != cudaSuccess) return e;
-        g_scratch_addr[dev].store(p, std::memory_order_release);
+    *bytes = kScratchBytes;
+    std::lock_guard<std::mutex> lock(g_cache_mutex);
+    Cached& c = g_cache[dev];
+    unsigned long long id = 0;
+    if (c.addr && current_context_id(&id) && id == c.ctx_id) {
+        *out = c.addr;
+        return cudaSuccess;
+    }
+    void* p = nullptr;
+    e = cudaGetSymbolAddress(&p, g_sign_scratch);   // makes the device's context current
+    if (e != cudaSuccess) return e;
+    if (current_context_id(&id)) {
+        c.ctx_id = id;
+        c.addr = p;
+    } else {
+        c.addr = nullptr;    // no id to check a cached address against: look it up on every call
     }
     *out = p;
     return cudaSuccess;
@@ -48,23 +97,14 @@ cudaError_t scratch_address(void** out) {
 
 }  // namespace
 
+// Every argument is checked first, exactly as for mr_reduce_scatter_sign_ef
+// (the same checks in the same order, so the same statuses; the messages name
+// this entry point); only then is the static scratch located and handed over
+// as the workspace.  It always holds the call's partials (see the
+// static_assert above).
 extern "C" mr_status_t mr_reduce_scatter_sign_ef_noalloc(const void* const* grad, void* const* err, void* const* recv,
                                                          float* scales, int W, size_t N, mr_op_t op, mr_algo_t algo,
                                                          void* stream) {
-    if (W >= 1 && W <= MR_MAX_RANKS && N > 0) {
-        const size_t need = mr_sign_ef_workspace_bytes(W, N);
-        if (need > kScratchBytes)
-            return mr::report_error(MR_ERR_INVALID_ARGUMENT,
-                                    "reduce_scatter_sign_ef_noalloc: W = %d, N = %zu needs %zu bytes of scratch; "
-                                    "the static scratch holds %zu (use mr_reduce_scatter_sign_ef with a workspace)",
-                                    W, N, need, kScratchBytes);
-        void* scratch = nullptr;
-        const cudaError_t e = scratch_address(&scratch);
-        if (e != cudaSuccess)
-            return mr::report_error(MR_ERR_CUDA, "reduce_scatter_sign_ef_noalloc: locating the static scratch failed: %s",
-                                    cudaGetErrorString(e));
-        return mr_reduce_scatter_sign_ef(grad, err, recv, scales, W, N, op, algo, scratch, kScratchBytes, stream);
-    }
-    // W out of range or nothing to do: the regular entry point reports it.
-    return mr_reduce_scatter_sign_ef(grad, err, recv, scales, W, N, op, algo, nullptr, 0, stream);
+    return mr::run_sign_ef("reduce_scatter_sign_ef_noalloc", mr::MODE_REDUCE_SCATTER, grad, err, recv, scales, W, N,
+                           op, algo, nullptr, 0, stream, scratch_address);
 }

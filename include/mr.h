@@ -148,12 +148,13 @@ mr_status_t mr_allreduce_rmsnorm(const void* const* send, void* const* recv, int
  * (fp32 only).  For every rank r and element e:
  *     p = grad[r][e] + err[r][e]                 (one fp32 add)
  *     s_r = ||p_r||_1 / N                        (L1 norm of the whole rank
- *                                                 buffer: per-thread compensated
- *                                                 fp32 sums, an fp64 tree per
- *                                                 block, the block partials
- *                                                 added in order in fp64, one
- *                                                 fp64 divide, one rounding to
- *                                                 fp32 -- the same on every run)
+ *                                                 buffer over N: the exact sum
+ *                                                 of the |p| divided exactly by
+ *                                                 N, rounded once to the nearest
+ *                                                 fp32, ties to even -- a
+ *                                                 function of the data alone;
+ *                                                 NaN if any p is NaN, else +inf
+ *                                                 if any |p| is infinite)
  *     q = +s_r if p >= 0 else -s_r               (the 1-bit code, decoded)
  *     err[r][e] = p - q                          (what was not sent: carried to
  *                                                 the next step)
@@ -167,10 +168,11 @@ mr_status_t mr_allreduce_rmsnorm(const void* const* send, void* const* recv, int
  *   grad[r]: N elements (read); err[r]: N elements (read, then overwritten);
  *   scales: W floats of device memory, receives s_r (may be NULL);
  *   workspace: device memory of at least mr_sign_ef_workspace_bytes(W, N)
- *   bytes, owned by the caller, 8-byte aligned; its contents need no
- *   initialisation and are scratch after the call.  Calls that share a
- *   workspace must not run concurrently.  Other ops return
- *   MR_ERR_UNSUPPORTED.  Two kernels are launched on `stream`.
+ *   bytes (at most 90112 for any W and N), owned by the caller, 8-byte
+ *   aligned; its contents need no initialisation and are scratch after the
+ *   call.  Calls that share a workspace must not run concurrently.  Other ops
+ *   return MR_ERR_UNSUPPORTED; N >= 2^37 returns MR_ERR_INVALID_ARGUMENT.
+ *   Two kernels are launched on `stream`.
  * [SIGN] "Communication Optimization: Gradient Compression, NCCL ..."
  * (mbrenndoerfer.com): 1-bit SGD sends sign(g) with the scale ||g||_1 / d;
  * error feedback compresses g plus the residual owed from the previous step
@@ -192,14 +194,14 @@ mr_status_t mr_reduce_scatter_sign_ef(const void* const* grad, void* const* err,
  * cudaMalloc's implicit synchronisation.  The pages have no counterpart: this
  * is an interface variant, not part of the method.
  *   Same arguments, results and errors as mr_reduce_scatter_sign_ef, without
- *   the workspace: the scratch is a 64 KiB array of device memory inside the
+ *   the workspace: the scratch is a 96 KiB array of device memory inside the
  *   library (every GPU that loads the library holds it until the process
- *   exits).  W * (blocks of N) partials must fit in it: every N for W <= 32,
- *   and up to 2^20 elements per rank at W = 64; larger requests return
- *   MR_ERR_INVALID_ARGUMENT and name the limit in mr_last_error().  Nothing
- *   here calls cudaMalloc, cudaFree or any allocating routine.
- *   The first call on each device looks up the array's device address (with
- *   that device current); make that first call before any stream capture.
+ *   exits).  That is more than any W and N need (at most 90112 bytes of
+ *   partials), so no size is refused for want of scratch.  Nothing here calls
+ *   cudaMalloc, cudaFree or any allocating routine.
+ *   The first call on each device (and the first after a device reset) looks
+ *   up the array's device address with that device current; make that first
+ *   call before any stream capture.
  *   Every call uses the same array: each call writes all the partials it
  *   later reads, so nothing needs clearing between calls, but calls that
  *   overlap on the GPU (other streams, other threads) race on it.

@@ -146,6 +146,62 @@ def test_valid_call_without_gpu_reports_cuda_error(mr):
     assert "launch failed" in mr.mr_last_error()
 
 
+def _sign_rs(lib, name, grad, err, recv, W, N, op=4, algo=0, workspace=None, ws_bytes=0):
+    args = [_arr(grad) if grad else None, _arr(err) if err else None, _arr(recv) if recv else None, None, W, N, op, algo]
+    if name == "mr_reduce_scatter_sign_ef":
+        args += [workspace, ws_bytes]
+    return getattr(lib, name)(*args, None)
+
+
+def test_sign_workspace_is_bounded(mr):
+    """At most 2048 partials of 11 words per call, whatever W and N: 90112
+    bytes, which the allocation-free entry point's 96 KiB array holds."""
+    lib = mr.load()
+    lib.mr_sign_ef_workspace_bytes.restype = ctypes.c_size_t
+    lib.mr_sign_ef_workspace_bytes.argtypes = [ctypes.c_int, ctypes.c_size_t]
+    worst = 0
+    for W in range(1, 65):
+        for N in (1, 8191, 8192, 8193, 1 << 20, 1 << 24, 1 << 36):
+            b = lib.mr_sign_ef_workspace_bytes(W, N)
+            assert b % 44 == 0 and b >= 44 * W
+            worst = max(worst, b)
+    assert worst == 2048 * 44 <= 96 * 1024
+    assert lib.mr_sign_ef_workspace_bytes(0, 100) == 0
+
+
+def test_sign_entry_points_check_arguments_alike(mr):
+    """The allocation-free entry point checks its arguments exactly as the
+    workspace one does, before anything touches the GPU: the same status for
+    every bad call (a NULL array or pointer, an unsupported op, N not divisible
+    by W, W out of range, N past 2^37), and nothing to do for N == 0."""
+    lib = mr.load()
+    base = 1 << 40
+    W, N = 4, 4096
+    g = [base + r * (1 << 20) for r in range(W)]
+    e = [base + (1 << 30) + r * (1 << 20) for r in range(W)]
+    o = [base + (1 << 31) + r * (1 << 20) for r in range(W)]
+    ws = base + (1 << 32)
+    cases = [
+        dict(grad=None, err=e, recv=o, W=W, N=N),
+        dict(grad=g, err=None, recv=o, W=W, N=N),
+        dict(grad=g, err=e[:3] + [0], recv=o, W=W, N=N),
+        dict(grad=g, err=e, recv=o, W=W, N=N, op=3),
+        dict(grad=g, err=e, recv=o, W=W, N=N, algo=7),
+        dict(grad=g, err=e, recv=o, W=W, N=N + 2),
+        dict(grad=g, err=e, recv=o, W=0, N=N),
+        dict(grad=g, err=e, recv=o, W=W, N=1 << 37),
+        dict(grad=g, err=[g[0]] + e[1:], recv=o, W=W, N=N),
+    ]
+    for c in cases:
+        a = _sign_rs(lib, "mr_reduce_scatter_sign_ef", workspace=ws, ws_bytes=1 << 20, **c)
+        b = _sign_rs(lib, "mr_reduce_scatter_sign_ef_noalloc", **c)
+        assert a == b != 0, c
+    assert _sign_rs(lib, "mr_reduce_scatter_sign_ef_noalloc", g, e, o, W, 0) == 0
+    # a valid call reaches the scratch lookup, which needs a GPU
+    assert _sign_rs(lib, "mr_reduce_scatter_sign_ef_noalloc", g, e, o, W, N) == 4
+    assert "static scratch" in mr.mr_last_error()
+
+
 def _cost_table():
     rows = []
     path = os.path.join(ROOT, "collective_reduction_math_gb300", "csrc", "cost_model.inc")

@@ -1,9 +1,9 @@
 """GPU parity of the 1-bit sign compression with error feedback.
 
-The scales are checked against the oracle's fp64 L1 norm to within one fp32
-unit (both round a nearly exact fp64 sum once; the orders differ).  Given the
-GPU's own scales, the oracle then reproduces the outputs and the new errors
-bit for bit.
+The scale is a function of the data alone (the exact mean magnitude rounded
+once to fp32), so the GPU's scales must equal the oracle's bit for bit, and
+the outputs and the new errors must equal what the oracle computes from its
+own scales, bit for bit.
 """
 import numpy as np
 import pytest
@@ -52,8 +52,8 @@ def run(mr, mode, op, algo, g, e, offset=0, steps=1):
         outs.check()
         s_gpu = scales.cpu().numpy()
         s_ref = oracle.sign_ef_scales(g, host_e)
-        assert np.all(np.abs(s_gpu - s_ref) <= np.spacing(s_ref)), (s_gpu, s_ref)
-        want, host_e = oracle.sign_ef_collective(mode, op, algo, g, host_e, s_gpu)
+        assert_same(s_gpu, s_ref, f"scales {mode} W={W} N={N}")
+        want, host_e = oracle.sign_ef_collective(mode, op, algo, g, host_e, s_ref)
         got = outs.host()
         if mode == "allreduce":
             for j in range(W):
@@ -86,6 +86,79 @@ def test_unaligned_and_repeated(mr, offset):
         g = synth.normal(70 + W, W, N, 1e-3, "fp32")
         e = [np.zeros(N, np.float32) for _ in range(W)]
         run(mr, "allreduce", "avg", "ring", g, e, offset=offset, steps=3)
+
+
+def _hard_scale_ranks():
+    """One rank per hand-worked case of the scale's exact rounding (ties,
+    a remainder that decides a tie, subnormal means, the largest
+    magnitudes, a mean an fp64 running sum would round the wrong way), each
+    padded with zeros to a common N, plus ranks drawn over every binade."""
+    two = 2.0
+    cases = [[3.0, 3 * two ** -24, 3 * two ** -100], [1.0, 1 + two ** -23], [1 + two ** -23, 1 + two ** -22],
+             [two ** -149, 0.0], [3 * two ** -149, 0.0], [2 * two ** -149, 0.0, 0.0],
+             [3 * two ** -125, two ** -147, 0.0], [3.4028234663852886e38] * 2, [-2.0, 2.0, -0.0, 0.0]]
+    return cases
+
+
+@pytest.mark.parametrize("N", [3, 8, 4099, 8 * 8192 + 5])
+def test_scales_exact_on_hard_cases(mr, N):
+    """Scales of hand-worked and every-binade data, bit for bit.  Zero
+    padding changes N but not the sum, so each case's mean is its own sum over
+    this N.  The values are split as g + e with e = 0, and also with e
+    carrying part of the value (the sum p = g + e is formed in fp32 on both
+    sides)."""
+    import oracle
+    import torch
+    rng = np.random.default_rng(N)
+    ranks = []
+    for c in _hard_scale_ranks():
+        if len(c) > N:
+            continue
+        p = np.zeros(N, np.float32)
+        p[:len(c)] = np.array(c, np.float32)
+        ranks.append(p)
+    for _ in range(3):
+        bits = rng.integers(0, 0x7F800000, size=N, dtype=np.uint32) | (rng.integers(0, 2, size=N, dtype=np.uint32) << np.uint32(31))
+        ranks.append(bits.view(np.float32).copy())
+        ranks.append((bits.view(np.float32) * np.float32(2.0 ** -110)).astype(np.float32))
+    W = len(ranks)
+    for split in (False, True):
+        if split:
+            e = [(p * np.float32(0.25)).astype(np.float32) for p in ranks]
+            g = [(p - x).astype(np.float32) for p, x in zip(ranks, e)]
+        else:
+            g, e = ranks, [np.zeros(N, np.float32) for _ in ranks]
+        gd = [to_device(x, "fp32") for x in g]
+        ed = [to_device(x, "fp32") for x in e]
+        out = [torch.empty(N, device="cuda") for _ in range(W)]
+        scales = torch.empty(W, device="cuda")
+        mr.mr_allreduce_sign_ef(gd, ed, out, scales=scales, op="sum", algo="ring")
+        torch.cuda.synchronize()
+        assert_same(scales.cpu().numpy(), oracle.sign_ef_scales(g, e), f"hard scales N={N} split={split}")
+
+
+def test_scales_of_non_finite_values(mr):
+    """An infinite |p| makes its rank's scale +inf, a NaN makes it NaN (and
+    wins over an infinity); the other ranks are unaffected."""
+    import oracle
+    import torch
+    N = 4096
+    g = [np.full(N, 0.5, np.float32) for _ in range(4)]
+    g[1][17] = np.inf
+    g[2][100] = -np.inf
+    g[2][200] = np.nan
+    e = [np.zeros(N, np.float32) for _ in range(4)]
+    gd = [to_device(x, "fp32") for x in g]
+    ed = [to_device(x, "fp32") for x in e]
+    out = [torch.empty(N, device="cuda") for _ in range(4)]
+    scales = torch.empty(4, device="cuda")
+    mr.mr_allreduce_sign_ef(gd, ed, out, scales=scales, op="sum", algo="ring")
+    torch.cuda.synchronize()
+    got = scales.cpu().numpy()
+    want = oracle.sign_ef_scales(g, e)
+    assert got[0] == want[0] == np.float32(0.5) and got[3] == np.float32(0.5)
+    assert np.isposinf(got[1]) and np.isposinf(want[1])
+    assert np.isnan(got[2]) and np.isnan(want[2])
 
 
 def test_workload_full(mr):

@@ -34,8 +34,10 @@ def _ptrs(ts):
     return (ctypes.c_void_p * len(ts))(*[t.data_ptr() for t in ts])
 
 
+# The last case needs the most partials any call can have (64 ranks x 32
+# blocks), which the library's array must hold.
 @pytest.mark.parametrize("W,N,op,algo", [(8, 8 * 50000, "avg", "ring"), (5, 5 * 1001, "sum", "tree"),
-                                         (32, 32 * (1 << 16), "avg", "ring")])
+                                         (64, 1 << 18, "avg", "ring")])
 def test_noalloc_matches_workspace_entry_point(mr, W, N, op, algo):
     import torch
     lib = mr.load()
@@ -61,17 +63,3 @@ def test_noalloc_matches_workspace_entry_point(mr, W, N, op, algo):
             assert torch.equal(err_a[k], err_b[k]), f"call {call}: residual {k} differs"
     # the second call really continued from the first one's residuals
     assert not np.array_equal(err_b[0].cpu().numpy(), e0[0])
-
-
-def test_noalloc_rejects_oversize(mr):
-    """W = 64 with 2^21 elements per rank needs 128 KiB of partials: refused,
-    with the limit named, before anything reaches the GPU.  (One shared
-    buffer stands in for every pointer; the alias check would refuse it too.)"""
-    import torch
-    lib = mr.load()
-    buf = torch.zeros(16, device="cuda")
-    ps = (ctypes.c_void_p * 64)(*([buf.data_ptr()] * 64))
-    st = lib.mr_reduce_scatter_sign_ef_noalloc(ps, ps, ps, None, 64, 64 << 21, mr.OPS["avg"], 0,
-                                               torch.cuda.current_stream().cuda_stream)
-    assert st == 1
-    assert "static scratch" in mr.mr_last_error()
