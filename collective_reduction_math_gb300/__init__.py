@@ -20,7 +20,7 @@ __all__ = [
     "mr_allreduce", "mr_reduce_scatter", "mr_all_gather", "mr_allreduce_ex", "mr_reduce_scatter_ex", "mr_allreduce_rmsnorm", "mr_allreduce_sign_ef",
     "mr_reduce_scatter_sign_ef", "mr_reduce_scatter_sign_ef_noalloc", "mr_sign_ef_workspace_bytes",
     "mr_status_string", "mr_last_error",
-    "mr_allreduce_ptrs", "mr_plan_auto", "mr_plan_ring_order", "mr_plan_tree", "mr_chunk_lo", "mr_launch_count", "MRError",
+    "mr_allreduce_ptrs", "mr_plan_auto", "mr_plan_ring_order", "mr_plan_tree", "mr_chunk_lo", "mr_launch_count", "mr_launch_floor", "MRError",
     "load", "LIB_PATH",
     "DTYPES", "OPS", "ALGOS", "MAX_RANKS",
 ]
@@ -90,6 +90,8 @@ def load():
     L.mr_plan_auto.restype = i
     L.mr_launch_count.argtypes = []
     L.mr_launch_count.restype = ctypes.c_ulonglong
+    L.mr_launch_floor.argtypes = [ctypes.c_uint, vp]
+    L.mr_launch_floor.restype = i
     _lib = L
     return L
 
@@ -333,3 +335,10 @@ def mr_chunk_lo(W: int, N: int, k: int) -> int:
 
 def mr_launch_count() -> int:
     return int(load().mr_launch_count())
+
+
+def mr_launch_floor(ctas: int = 1, stream=None):
+    """One empty kernel of ``ctas`` CTAs on the stream (the launch floor)."""
+    st = load().mr_launch_floor(ctas, _stream(stream))
+    if st:
+        _raise(st)

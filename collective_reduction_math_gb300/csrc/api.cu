@@ -323,6 +323,10 @@ mr_status_t run_reduce(const char* what, int mode, const void* const* send, void
 }  // namespace
 
 namespace mr {
+// A kernel that does nothing but enter and leave like every other kernel here
+// (the programmatic-dependent-launch wait and signal): the launch floor.
+__global__ void __launch_bounds__(kThreads) empty_kernel(int) { pdl_enter(); }
+
 bool pdl_enabled() {
     static const bool on = [] {
         const char* e = getenv("MR_PDL");
@@ -747,5 +751,14 @@ size_t mr_chunk_lo(int W, size_t N, int k) {
 }
 
 unsigned long long mr_launch_count(void) { return g_launches.load(std::memory_order_relaxed); }
+
+mr_status_t mr_launch_floor(unsigned ctas, void* stream) {
+    g_last_error.clear();
+    if (ctas < 1 || ctas > 65535) return fail(MR_ERR_INVALID_ARGUMENT, "mr_launch_floor: ctas = %u is outside [1, 65535]", ctas);
+    const cudaError_t e = mr::launch_kernel(mr::empty_kernel, dim3(ctas, 1, 1), 0, (cudaStream_t)stream, 0, 0);
+    if (e != cudaSuccess) return fail(MR_ERR_CUDA, "launch_floor launch failed: %s", cudaGetErrorString(e));
+    g_launches.fetch_add(1, std::memory_order_relaxed);
+    return MR_OK;
+}
 
 }  // extern "C"

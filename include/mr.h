@@ -289,6 +289,17 @@ size_t mr_chunk_lo(int W, size_t N, int k);
  * all devices).  Lets a caller count the GPU launches inside a timed region. */
 unsigned long long mr_launch_count(void);
 
+/*
+ * mr_launch_floor: launch one empty kernel of `ctas` CTAs (1..65535) of the
+ * library's block size on `stream`, with the launch attributes every kernel
+ * here gets (programmatic dependent launch unless MR_PDL=0).  It reads and
+ * writes nothing.  Timed beside a small collective, it separates the cost of
+ * a launch from the kernel's own work.  The pages have no counterpart: this
+ * is a measuring aid.  Returns MR_ERR_INVALID_ARGUMENT for ctas out of
+ * range, MR_ERR_CUDA if the launch fails; counts in mr_launch_count().
+ */
+mr_status_t mr_launch_floor(unsigned ctas, void* stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -145,12 +145,18 @@ def draw(dist, seed: int, W: int, N: int, dtype: str, tag: int = TAG_GRAD):
     raise ValueError(kind)
 
 
-def workload_inputs(name: str, seed: int = 0, N: int | None = None):
-    """The rank buffers of a named workload (N overrides the size, for sweeps
-    and for bounded samples)."""
+def workload_inputs(name: str, seed: int = 0, N: int | None = None, W: int | None = None,
+                    dtype: str | None = None):
+    """The rank buffers of a named workload.  N overrides the size (for sweeps
+    and bounded samples); W and dtype override the rank count and the element
+    type, keeping the workload's distribution (an integer distribution is
+    needed for int32)."""
     w = WORKLOADS[name]
     n = N if N is not None else w["N"]
-    return draw(w["dist"], seed, w["W"], n, w["dtype"], TAG_GRAD)
+    dt = dtype or w["dtype"]
+    if dt == "int32" and w["dist"][0] != "uniform_int":
+        raise ValueError(f"{name} draws floats; int32 needs an integer workload")
+    return draw(w["dist"], seed, W or w["W"], n, dt, TAG_GRAD)
 
 
 def workload_param_shards(name: str, seed: int = 0, N: int | None = None):

@@ -202,6 +202,15 @@ def test_sign_entry_points_check_arguments_alike(mr):
     assert "static scratch" in mr.mr_last_error()
 
 
+def test_launch_floor_arguments(mr):
+    lib = mr.load()
+    assert lib.mr_launch_floor(0, None) == 1
+    assert lib.mr_launch_floor(65536, None) == 1
+    assert "ctas" in mr.mr_last_error()
+    assert lib.mr_launch_floor(1, None) == 4        # no GPU here: the launch itself fails
+    assert "launch failed" in mr.mr_last_error()
+
+
 def _cost_table():
     rows = []
     path = os.path.join(ROOT, "collective_reduction_math_gb300", "csrc", "cost_model.inc")

@@ -60,7 +60,9 @@ CASES = [("small_int_fp32_w2", None, None, lambda W, N, b: 2 * W * N * b),
          ("int_counts_w16", None, 16 * 64, lambda W, N, b: 2 * W * N * b),
          ("sign_ef_fp32_w8", None, 8 * 1000, lambda W, N, b: 5 * W * N * b + N * b),
          ("sign_ef_fp32_w8", "allreduce_sign_ef", 8 * 1000, lambda W, N, b: 5 * W * N * b + W * N * b),
-         ("tp_decode_rmsnorm_bf16_w8", None, None, lambda W, N, b: (2 * W + 2) * N * b + 8192 * b)]
+         ("tp_decode_rmsnorm_bf16_w8", None, None, lambda W, N, b: (2 * W + 2) * N * b + 8192 * b),
+         ("tp_decode_rmsnorm_bf16_w8", "allreduce_then_rmsnorm", None,
+          lambda W, N, b: (2 * W + 2) * N * b + 8192 * b)]
 
 
 @pytest.mark.parametrize("workload,collective,n,bytes_of", CASES)
@@ -83,3 +85,31 @@ def test_step_buffers_and_bytes(bench, workload, collective, n, bytes_of):
     assert not any(t.data_ptr() in old for t in ins + outs)
     assert [t.numel() for t in ins] == [t.numel() for t in S.e2e_in]
     assert [t.numel() for t in outs] == [t.numel() for t in S.e2e_out]
+
+
+@pytest.mark.parametrize("ranks,dtype", [(10, None), (12, "bf16"), (3, "fp32")])
+def test_rank_and_dtype_overrides(bench, ranks, dtype):
+    import torch
+    args = argparse.Namespace(workload="sweep_fp32_w8", collective=None, op=None, algo="tree", group=None,
+                              per_hop=False, n=4096, ranks=ranks, dtype=dtype)
+    S = bench.Step(args, FakeLibrary(), torch, torch.device("cpu"))
+    assert S.W == ranks and len(S.xs) == ranks and S.dtype == (dtype or "fp32")
+    assert S.bytes == 2 * ranks * 4096 * (2 if dtype == "bf16" else 4)
+    cfg = S.config("one call per step")
+    assert cfg["W"] == ranks and cfg["algo"] == "tree"
+    with pytest.raises(ValueError):
+        synth.workload_inputs("sweep_fp32_w8", N=16, dtype="int32")     # a float workload has no int32 form
+
+
+def test_both_arms_report_the_same_config(bench):
+    """The reference arm's config is the GPU arm's for the headline workload,
+    key for key (N_timed tells a sampled run apart)."""
+    import torch
+    args = argparse.Namespace(workload=bench.WORKLOAD, collective=None, op=None, algo="ring", group=None,
+                              per_hop=False, n=8 * 1024)
+    S = bench.Step(args, FakeLibrary(), torch, torch.device("cpu"))
+    gpu = S.config("one call per step")
+    W, N = S.W, S.N
+    ref = bench.config_dict(bench.WORKLOAD, "allreduce", W, N, "fp32", "avg", "ring", None, False, 2 * W * N * 4,
+                            gpu["l2"], N, "one call per step")
+    assert gpu == ref

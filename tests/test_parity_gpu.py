@@ -223,6 +223,26 @@ def test_side_stream_and_launch_count(mr):
         assert_same(y.cpu().numpy(), want, "side stream")
 
 
+def test_launch_floor_runs_between_calls(mr):
+    """The empty kernel launches (1 CTA and a full grid), counts as a launch,
+    and leaves the calls queued around it on the stream exact."""
+    import oracle
+    import torch
+    W, N = 4, 4096 + 3
+    host = synth.normal(6001, W, N, 1.0, "fp32")
+    xs = [to_device(h, "fp32") for h in host]
+    ys = [torch.empty_like(x) for x in xs]
+    before = mr.mr_launch_count()
+    mr.mr_launch_floor(1)
+    mr.mr_allreduce(xs, ys, op="sum", algo="tree")
+    mr.mr_launch_floor(3 * torch.cuda.get_device_properties(0).multi_processor_count)
+    torch.cuda.synchronize()
+    assert mr.mr_launch_count() == before + 3
+    want = oracle.allreduce("fp32", "sum", "tree", host)
+    for y in ys:
+        assert_same(y.cpu().numpy(), want, "around the empty kernel")
+
+
 def test_denormals_and_signed_zero(mr):
     """Subnormal inputs add exactly (no flush to zero) on both sides."""
     W, N = 4, 4096
