@@ -146,16 +146,34 @@ constexpr int reduce_unroll_for(int wcap, bool rs) {
     return wcap == 2 ? 4 : wcap == 4 ? 2 : (wcap == 8 && rs) ? 2 : 1;
 }
 constexpr int reduce_unroll(int W, bool rs) { return reduce_unroll_for(reduce_wcap(W), rs); }
-constexpr int reduce_blocks_per_sm(int wcap, int u) { return (wcap <= 8 && wcap * u <= 8) ? 3 : 2; }
-// 13 to 16 ranks fold in batches of 8 (as above 16 ranks), which frees the
-// registers that 16 live vectors and 16 pointers take; measured on GB300 at
-// W = 16 (TB/s, plain -> batched): fp32 ring 5.4 -> 6.2, fp32 tree 6.3 -> 6.5,
-// bf16 tree 4.8 -> 6.4, int32 tree 5.8 -> 6.0, per-hop bf16 avg tree 6.0 ->
-// 6.4, rings otherwise within 2 %.  At W = 12 the second batch is half empty
-// and the plain fold stays ahead, except for the bf16 tree, whose plain fold
-// spills there (W = 10 / 12 bf16 tree avg 4.1 -> 5.1 / 4.6 -> 5.6 TB/s
-// batched): it folds in batches from 9 ranks.
+// Resident CTAs per SM (the kernel's launch bounds and the grid's size): 3 for
+// the all-reduce up to 8 ranks and for the 16-slot batched folds (8 vectors
+// live at a time), else 2.  At 2 per SM the batched W = 16 folds sat at 24 %
+// of warps active, stalled on loads (ncu, int32 W = 16: 74 % of DRAM peak).
+constexpr int reduce_blocks_per_sm(int wcap, int u, bool batch) {
+    return ((wcap <= 8 && wcap * u <= 8) || (batch && wcap == 16)) ? 3 : 2;
+}
+// Whether the reduce kernel for (W, order, element type, per-hop rounding)
+// folds in batches of 8: only 8 vectors and no pointers live in registers, so
+// it runs at 3 CTAs per SM (16 slots) where the plain 16-slot fold runs at 2.
+// Measured on GB300 at 32 MiB per rank (TB/s, plain -> batched):
+//   tree from 9 ranks, every element type: fp32 max W = 9 4.63 -> 6.13,
+//     int32 sum W = 11 5.04 -> 5.88, int32 max W = 12 5.90 -> 6.23;
+//   rings (and the hierarchical order) at 9 to 11 ranks: bf16 max W = 9
+//     5.58 -> 5.92, per-hop bf16 avg W = 10 5.26 -> 6.21;
+//   at 12 ranks the plain ring stays 1-3.5 % ahead (bf16 max 6.23 against
+//     6.01), except per-hop (5.75 -> 6.03);
+//   from 13 ranks every order batched (at W = 16 with 3 CTAs per SM: int32
+//     sum ring 5.88 -> 6.28 at 16 MiB per rank, per-hop bf16 ring 6.10 ->
+//     6.37).
 constexpr int kBatchFromRanks = 13;
+constexpr bool reduce_batched(int W, int algo, int dtype, bool hop) {
+    (void)dtype;
+    if (W >= kBatchFromRanks) return true;
+    if (W <= 8) return false;
+    if (algo == MR_TREE) return true;
+    return W < 12 || hop;
+}
 
 // ---------------------------------------------------------------------------
 // Programmatic dependent launch.  Every kernel of the library is launched with

@@ -374,7 +374,7 @@ __device__ __forceinline__ int order_rank(int W, const Segment& sg, int i, int g
 }
 
 template <int DT, int OP, int ALGO, int WCAP, int VB, int U, bool HOP, bool BATCH>
-__global__ void __launch_bounds__(kThreads, reduce_blocks_per_sm(WCAP, U))
+__global__ void __launch_bounds__(kThreads, reduce_blocks_per_sm(WCAP, U, BATCH))
 reduce_kernel(const __grid_constant__ ReduceParams P) {
     using A = Arith<DT, OP>;
     using raw_t = typename A::raw_t;
@@ -722,7 +722,7 @@ cudaError_t launch_reduce(const ReduceParams& P, int op, dim3 grid, cudaStream_t
                 if (rs) return launch_kernel(reduce_kernel<DT, OP, ALGO, 8, 16, reduce_unroll_for(8, true), HOP, false>, grid, 0, stream, 0, P);
                 return launch_kernel(reduce_kernel<DT, OP, ALGO, 8, 16, reduce_unroll_for(8, false), HOP, false>, grid, 0, stream, 0, P);
             case 16:
-                if (P.W >= kBatchFromRanks || (DT == MR_BF16 && ALGO == MR_TREE))
+                if (reduce_batched(P.W, ALGO, DT, HOP))
                     return launch_kernel(reduce_kernel<DT, OP, ALGO, 16, 16, 1, HOP, true>, grid, 0, stream, 0, P);
                 return launch_kernel(reduce_kernel<DT, OP, ALGO, 16, 16, reduce_unroll_for(16, false), HOP, false>, grid, 0, stream, 0, P);
             default:

@@ -47,7 +47,7 @@ def check(mr, dtype, op, algo, group, hop, W, N):
             assert_same(o, want_rs[k], f"reduce_scatter_ex {dtype} {op} {algo} g={group} hop={hop} shard {k}")
 
 
-@pytest.mark.parametrize("W,group", [(2, 1), (4, 2), (6, 3), (8, 2), (8, 4), (12, 4), (16, 4), (16, 8), (24, 6),
+@pytest.mark.parametrize("W,group", [(2, 1), (4, 2), (6, 3), (8, 2), (8, 4), (10, 5), (12, 4), (16, 4), (16, 8), (24, 6),
                                      (64, 8)])
 @pytest.mark.parametrize("dtype", ["fp32", "bf16", "int32"])
 def test_hier_parity(mr, W, group, dtype):
@@ -57,7 +57,7 @@ def test_hier_parity(mr, W, group, dtype):
 
 
 @pytest.mark.parametrize("algo,group", [("ring", None), ("tree", None), ("hier", 4)])
-@pytest.mark.parametrize("W", [2, 8, 16, 40])
+@pytest.mark.parametrize("W", [2, 8, 10, 12, 16, 40])
 def test_per_hop_bf16_parity(mr, algo, group, W):
     if algo == "hier" and W % 4:
         group = 2

@@ -108,9 +108,10 @@ def _sizes(W):
     return [1, 7, W * per + 13, W * per * 2]
 
 
-# W = 11 runs the plain fold with 16 register slots, 13 and 16 the batched
-# fold, 17 and up the batched fold with 64 slots
-CASES = [(W, N) for W in (1, 2, 3, 5, 8, 11, 13, 16, 17, 33, 64) for N in _sizes(W)]
+# W = 9 to 11 run the batched fold with 16 slots for every order, W = 12 the
+# plain 16-slot fold for the ring and the batched one for the tree, 13 and 16
+# the batched fold, 17 and up the batched fold with 64 slots
+CASES = [(W, N) for W in (1, 2, 3, 5, 8, 9, 11, 12, 13, 16, 17, 33, 64) for N in _sizes(W)]
 
 
 @pytest.mark.parametrize("W,N", CASES)
