@@ -480,6 +480,11 @@ mr_status_t mr_reduce_scatter_ex(const void* const* send, void* const* recv, int
                       hop);
 }
 
+// Shared memory a fused-RMSNorm CTA of a multi-CTA cluster reserves, so that
+// no more than two fit on one SM (228 KB of shared memory per SM, 1 KB of it
+// reserved per CTA).
+constexpr size_t kNormSpreadSmem = 80 * 1024;
+
 mr_status_t mr_allreduce_rmsnorm(const void* const* send, void* const* recv, int W, size_t rows, size_t hidden,
                                  const void* residual, void* residual_out, const void* weight, float eps,
                                  mr_dtype_t dtype, mr_algo_t algo, void* stream) {
@@ -548,7 +553,13 @@ mr_status_t mr_allreduce_rmsnorm(const void* const* send, void* const* recv, int
         csize *= 2;
     P.csize = csize;
     const size_t slice = (hidden + csize - 1) / csize + lanes;
-    const size_t smem = ((slice * 4 + 15) / 16) * 16;
+    // The row slice in shared memory.  Spread over a cluster (few rows), a
+    // CTA also reserves enough shared memory that at most two of them share
+    // an SM: three of the 256 decode CTAs on one SM left it with half as much
+    // again to load and store as the rest (per-phase timestamps, W = 8, 64 x
+    // 8192 bf16: 5.97 against 5.50 us per step).
+    size_t smem = ((slice * 4 + 15) / 16) * 16;
+    if (csize > 1) smem = std::max<size_t>(smem, kNormSpreadSmem);
     // One whole wave of resident CTAs, looping over the rows.  Residency is
     // the smaller of what the kernel's register budget allows (3 per SM up to
     // 8 ranks, 2 up to 16, else 1: its launch bounds) and what shared memory

@@ -62,6 +62,8 @@ struct NormParams {
 
 // Largest row the fused RMSNorm keeps in shared memory (fp32 per element).
 constexpr uint64_t kMaxNormHidden = 49152;
+// Most CTAs in one of its clusters (one row spread over up to 8 SMs).
+constexpr int kMaxNormCluster = 8;
 
 // 1-bit sign compression with error feedback (fp32).
 struct SignParams {

@@ -13,15 +13,20 @@
 //           shared memory, and accumulate h*h into a per-thread fp32
 //           partial (increasing element order);
 //   reduce  the partials with a fixed tree (warp shuffles, then the warp
-//           totals), then the C slice totals in cluster-rank order, read
-//           from each CTA's shared memory over the cluster (DSMEM), so every
-//           CTA -- and every run -- gets the same value;
+//           totals) into the CTA's slice total, which it pushes into every
+//           cluster peer's shared memory (DSMEM stores) before the cluster
+//           barrier; then every thread adds the C slice totals in
+//           cluster-rank order from its own CTA's copies, so every CTA -- and
+//           every run -- gets the same value;
 //           inv = 1 / sqrt(ss / hidden + eps), each step one IEEE operation;
 //   pass 2  out = (h * inv) * weight, rounded once, stored to all W outputs;
 //           residual_out gets h rounded once, from the same fp32 h.  Pass 1
 //           stores nothing to global memory, so the cluster barrier between
 //           the passes has no stores to wait for, and each thread's first
 //           weight vector is loaded once, before the first row.
+// Whatever depends on the parameters alone (the first row's segment and the
+// addresses of each thread's first vector) is worked out before the kernel
+// waits on the one before it.
 // Bytes per row: W reads and W writes of the row, plus the residual read,
 // residual_out write and weight read (the weight stays in L2 across rows).
 #include <cooperative_groups.h>
@@ -39,7 +44,6 @@ namespace mr {
 template <int DT, int ALGO, int WCAP, int VB>
 __global__ void __launch_bounds__(kThreads, WCAP <= 8 ? 3 : WCAP <= 16 ? 2 : 1)
 allreduce_rmsnorm_kernel(const __grid_constant__ NormParams P) {
-    pdl_enter();
     using A = Arith<DT, MR_SUM>;
     using raw_t = typename A::raw_t;
     constexpr int EB = Elem<DT>::kBytes;
@@ -49,8 +53,7 @@ allreduce_rmsnorm_kernel(const __grid_constant__ NormParams P) {
     extern __shared__ float4 row_smem[];
     float* hs = reinterpret_cast<float*>(row_smem);      // this CTA's slice of the row's fp32 h
     __shared__ float warp_part[kThreads / 32];
-    __shared__ float slice_total[2];                     // read by the cluster's peers, by row parity
-    __shared__ float inv_shared;
+    __shared__ float slice_total[2][kMaxNormCluster];    // [row parity][cluster rank], pushed by each CTA
 
     const int W = P.W;
     const uint64_t H = P.hidden;
@@ -98,6 +101,77 @@ allreduce_rmsnorm_kernel(const __grid_constant__ NormParams P) {
         if (P.residual) h = __fadd_rn(h, A::read(__ldg(static_cast<const raw_t*>(P.residual) + e), 0.0f));
         return h;
     };
+    // The h of one whole vector from its W loaded contributions (pass 1).
+    auto vector_h = [&](uint64_t e0, const Vec<VB> (&raw)[WCAP], float (&hv)[LANES]) {
+        Vec<VB> rv;
+        if (P.residual) rv = load_vec<VB>(static_cast<const char*>(P.residual) + e0 * EB);
+#pragma unroll
+        for (int l = 0; l < LANES; ++l) {
+            float y[WCAP];
+#pragma unroll
+            for (int i = 0; i < WCAP; ++i)
+                if (i < W) y[i] = A::read(get_lane<raw_t, VB>(raw[i], l), 0.0f);
+            float h = fold<A, ALGO, WCAP>(y, W);
+            if (P.residual) h = __fadd_rn(h, A::read(get_lane<raw_t, VB>(rv, l), 0.0f));
+            hv[l] = h;
+        }
+    };
+    // Adds a vector's h*h to the thread's partial and keeps h in the slice.
+    auto keep = [&](uint64_t sv, const float (&hv)[LANES], float& ss) {
+#pragma unroll
+        for (int l = 0; l < LANES; ++l) ss = __fadd_rn(ss, __fmul_rn(hv[l], hv[l]));
+        if constexpr (LANES % 4 == 0) {
+#pragma unroll
+            for (int q = 0; q < LANES / 4; ++q)
+                row_smem[sv * (LANES / 4) + q] = make_float4(hv[4 * q], hv[4 * q + 1], hv[4 * q + 2], hv[4 * q + 3]);
+        } else {
+#pragma unroll
+            for (int l = 0; l < LANES; ++l) hs[sv * LANES + l] = hv[l];
+        }
+    };
+
+    // Before waiting on the previous kernel, everything that depends on the
+    // parameters alone: the first row's segment and, up to 16 ranks, the W
+    // addresses of this thread's first vector.  Its loads then issue the
+    // moment the wait returns, instead of after a chain of parameter reads
+    // (measured with per-phase timestamps at decode size: pass 1 ended 2.7 us
+    // after the wait, most of it before the first load).
+    constexpr bool kPre = WCAP <= 16;
+    const char* pre[kPre ? WCAP : 1];
+    bool pre_ok = false;
+    int sgi_first = 0, sgi_pre = 0;
+    if (first_row < P.rows) {
+        const uint64_t base = first_row * H;
+        sgi_first = segment_near(base + (P.vec ? v_lo * LANES : c_lo));
+        if constexpr (kPre) {
+            const uint64_t v = v_lo + threadIdx.x;
+            if (P.vec && v < v_hi) {
+                const uint64_t e0 = base + v * LANES;
+                sgi_pre = segment_at(e0, sgi_first);
+                if (e0 + LANES <= P.seg[sgi_pre].hi) {
+                    pre_ok = true;
+#pragma unroll
+                    for (int i = 0; i < WCAP; ++i)
+                        if (i < W) pre[i] = input(P.seg[sgi_pre], i) + e0 * EB;
+                }
+            }
+        }
+    }
+    pdl_enter();
+
+    // The first row's first vector, from those addresses (its h*h opens the
+    // thread's partial for that row).
+    float ss_first = 0.0f;
+    if (kPre && pre_ok) {
+        const uint64_t e0 = first_row * H + (v_lo + threadIdx.x) * LANES;
+        Vec<VB> raw[WCAP];
+#pragma unroll
+        for (int i = 0; i < WCAP; ++i)
+            if (i < W) raw[i] = load_vec<VB>(pre[i]);
+        float hv[LANES];
+        vector_h(e0, raw, hv);
+        keep(threadIdx.x, hv, ss_first);
+    }
 
     // This thread's first pass-2 weight vector: the same for every row.
     Vec<VB> w_first;
@@ -107,14 +181,15 @@ allreduce_rmsnorm_kernel(const __grid_constant__ NormParams P) {
     int parity = 0;
     for (uint64_t row = first_row; row < P.rows; row += row_stride, parity ^= 1) {
         const uint64_t base = row * H;
-        int sgi = segment_near(base + (P.vec ? v_lo * LANES : c_lo));
-        float ss = 0.0f;
+        const bool peeled = kPre && pre_ok && row == first_row;     // its first vector is done
+        int sgi = row != first_row ? segment_near(base + (P.vec ? v_lo * LANES : c_lo))
+                : peeled ? sgi_pre : sgi_first;
+        float ss = peeled ? ss_first : 0.0f;
 
         // ---- pass 1 -------------------------------------------------------
         if (P.vec) {
-            for (uint64_t v = v_lo + threadIdx.x; v < v_hi; v += kThreads) {
+            for (uint64_t v = v_lo + threadIdx.x + (peeled ? kThreads : 0); v < v_hi; v += kThreads) {
                 const uint64_t e0 = base + v * LANES;
-                const uint64_t sv = v - v_lo;      // slot in this CTA's slice
                 sgi = segment_at(e0, sgi);
                 float hv[LANES];
                 if (e0 + LANES <= P.seg[sgi].hi) {
@@ -123,33 +198,13 @@ allreduce_rmsnorm_kernel(const __grid_constant__ NormParams P) {
 #pragma unroll
                     for (int i = 0; i < WCAP; ++i)
                         if (i < W) raw[i] = load_vec<VB>(input(sg, i) + e0 * EB);
-                    Vec<VB> rv;
-                    if (P.residual) rv = load_vec<VB>(static_cast<const char*>(P.residual) + e0 * EB);
-#pragma unroll
-                    for (int l = 0; l < LANES; ++l) {
-                        float y[WCAP];
-#pragma unroll
-                        for (int i = 0; i < WCAP; ++i)
-                            if (i < W) y[i] = A::read(get_lane<raw_t, VB>(raw[i], l), 0.0f);
-                        float h = fold<A, ALGO, WCAP>(y, W);
-                        if (P.residual) h = __fadd_rn(h, A::read(get_lane<raw_t, VB>(rv, l), 0.0f));
-                        hv[l] = h;
-                    }
+                    vector_h(e0, raw, hv);
                 } else {
                     // the vector straddles a chunk (or tree) boundary
 #pragma unroll
                     for (int l = 0; l < LANES; ++l) hv[l] = element_h(e0 + l, segment_at(e0 + l, sgi));
                 }
-#pragma unroll
-                for (int l = 0; l < LANES; ++l) ss = __fadd_rn(ss, __fmul_rn(hv[l], hv[l]));
-                if constexpr (LANES % 4 == 0) {
-#pragma unroll
-                    for (int q = 0; q < LANES / 4; ++q)
-                        row_smem[sv * (LANES / 4) + q] = make_float4(hv[4 * q], hv[4 * q + 1], hv[4 * q + 2], hv[4 * q + 3]);
-                } else {
-#pragma unroll
-                    for (int l = 0; l < LANES; ++l) hs[sv * LANES + l] = hv[l];
-                }
+                keep(v - v_lo, hv, ss);
             }
         } else {
             for (uint64_t i = c_lo + threadIdx.x; i < c_hi; i += kThreads) {
@@ -162,6 +217,15 @@ allreduce_rmsnorm_kernel(const __grid_constant__ NormParams P) {
         }
 
         // ---- the row's sum of squares, in a fixed tree ---------------------
+        // Warp shuffles, then the warp totals: this CTA's slice total, which
+        // warp 0 pushes into every cluster peer's slot for this CTA (a remote
+        // shared-memory store each; the cluster barrier's release makes them
+        // visible).  After the barrier every thread adds the C local slots in
+        // cluster-rank order, so every CTA -- and every run -- gets the same
+        // sum, with no remote read after the barrier.  The slots alternate by
+        // row parity, so a fast CTA's next row cannot overwrite a slot a peer
+        // is still reading: it would first need that peer at the next row's
+        // barrier.
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1) ss = __fadd_rn(ss, __shfl_down_sync(0xffffffffu, ss, o));
         if (lane == 0) warp_part[warp] = ss;
@@ -170,28 +234,17 @@ allreduce_rmsnorm_kernel(const __grid_constant__ NormParams P) {
             float t = lane < kThreads / 32 ? warp_part[lane] : 0.0f;
 #pragma unroll
             for (int o = 16; o > 0; o >>= 1) t = __fadd_rn(t, __shfl_down_sync(0xffffffffu, t, o));
-            if (lane == 0) {
-                if (C == 1) inv_shared = __fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(__fdiv_rn(t, (float)H), P.eps)));
-                else slice_total[parity] = t;
+            t = __shfl_sync(0xffffffffu, t, 0);
+            if (lane < C) {
+                if (C == 1) slice_total[parity][0] = t;
+                else *cluster.map_shared_rank(&slice_total[parity][crank], lane) = t;
             }
         }
-        if (C > 1) {
-            // Every CTA of the cluster adds the C slice totals in rank order.
-            // The totals alternate between two slots by row parity, so one
-            // cluster barrier per row keeps a fast CTA from overwriting a slot
-            // a peer is still reading.
-            cluster.sync();
-            if (warp == 0) {
-                // lane r reads CTA r's total (one round of remote reads), then
-                // lane 0 adds them in rank order
-                const float mine = lane < C ? *cluster.map_shared_rank(&slice_total[parity], lane) : 0.0f;
-                float t = 0.0f;
-                for (int r = 0; r < C; ++r) t = __fadd_rn(t, __shfl_sync(0xffffffffu, mine, r));
-                if (lane == 0) inv_shared = __fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(__fdiv_rn(t, (float)H), P.eps)));
-            }
-        }
-        __syncthreads();
-        const float inv = inv_shared;
+        if (C > 1) cluster.sync();
+        else __syncthreads();
+        float row_ss = 0.0f;
+        for (int r = 0; r < C; ++r) row_ss = __fadd_rn(row_ss, slice_total[parity][r]);
+        const float inv = __fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(__fdiv_rn(row_ss, (float)H), P.eps)));
 
         // ---- pass 2 -------------------------------------------------------
         if (P.vec) {
@@ -241,10 +294,9 @@ allreduce_rmsnorm_kernel(const __grid_constant__ NormParams P) {
         }
         __syncthreads();    // the row buffer and the partials are reused by the next row
     }
-    // Peers may still read this CTA's slice totals: leave together.  Each
-    // peer has consumed what it read before it arrives, so the arrive need
-    // not wait for this CTA's output stores (relaxed).
-    if (C > 1) asm volatile("barrier.cluster.arrive.relaxed.aligned;\n\tbarrier.cluster.wait.aligned;" ::: "memory");
+    // No barrier at exit: peers write into this CTA's shared memory only
+    // before a row's cluster barrier, which this CTA has passed, and never
+    // read it.
 }
 
 template <int DT, int ALGO, int WCAP, int VB>
