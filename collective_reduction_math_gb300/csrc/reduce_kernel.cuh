@@ -382,7 +382,6 @@ reduce_kernel(const __grid_constant__ ReduceParams P) {
     constexpr int EB = Elem<DT>::kBytes;
     constexpr int LANES = VB / EB;
 
-    pdl_enter();    // the previous kernel on the stream has finished with our buffers
 
     const int W = P.W;
     const float s = P.scale;
@@ -484,6 +483,24 @@ reduce_kernel(const __grid_constant__ ReduceParams P) {
         }
     };
 
+    // Before waiting on the previous kernel, whatever depends on the
+    // parameters alone: this CTA's first vector tile and its segment's input
+    // pointers (a 64-bit divide and a chain of parameter reads).  A small
+    // call is one tile per CTA, so its loads then issue as soon as the wait
+    // returns.
+    uint64_t t_first = blockIdx.x;
+    if (P.vec) {
+        const uint64_t ntiles = P.tiles_max * (uint64_t)P.nseg;
+        for (; t_first < ntiles; t_first += gridDim.x) {
+            const int s0 = (int)(t_first % (uint64_t)P.nseg);
+            if (t_first / (uint64_t)P.nseg < P.tile_start[s0 + 1] - P.tile_start[s0]) {
+                enter(s0);
+                break;
+            }
+        }
+    }
+    pdl_enter();    // the previous kernel on the stream has finished with our buffers
+
     int seg = 0;
     if (P.vec) {
         // Vector tiles are dealt round-robin across segments: tile t is tile
@@ -493,7 +510,7 @@ reduce_kernel(const __grid_constant__ ReduceParams P) {
         // one after another.
         const uint64_t ntiles = P.tiles_max * (uint64_t)P.nseg;
         constexpr uint64_t kTile = (uint64_t)kThreads * U;    // vectors per tile
-        for (uint64_t t = blockIdx.x; t < ntiles; t += gridDim.x) {
+        for (uint64_t t = t_first; t < ntiles; t += gridDim.x) {
             seg = (int)(t % (uint64_t)P.nseg);
             const uint64_t local = t / (uint64_t)P.nseg;
             if (local >= P.tile_start[seg + 1] - P.tile_start[seg]) continue;

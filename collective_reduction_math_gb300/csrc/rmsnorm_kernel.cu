@@ -12,12 +12,12 @@
 //           fp32), add the residual (one fp32 add), keep the fp32 h in
 //           shared memory, and accumulate h*h into a per-thread fp32
 //           partial (increasing element order);
-//   reduce  the partials with a fixed tree (warp shuffles, then the warp
-//           totals) into the CTA's slice total, which it pushes into every
-//           cluster peer's shared memory (DSMEM stores) before the cluster
-//           barrier; then every thread adds the C slice totals in
-//           cluster-rank order from its own CTA's copies, so every CTA -- and
-//           every run -- gets the same value;
+//   reduce  the partials with a fixed tree: warp shuffles give the warp
+//           partials, which each warp pushes into every cluster peer's shared
+//           memory (DSMEM stores) before the cluster barrier; then every
+//           thread adds, from its own CTA's copies, each CTA's warp partials
+//           in a fixed tree and the C slice totals in cluster-rank order, so
+//           every CTA -- and every run -- gets the same value;
 //           inv = 1 / sqrt(ss / hidden + eps), each step one IEEE operation;
 //   pass 2  out = (h * inv) * weight, rounded once, stored to all W outputs;
 //           residual_out gets h rounded once, from the same fp32 h.  Pass 1
@@ -49,11 +49,13 @@ allreduce_rmsnorm_kernel(const __grid_constant__ NormParams P) {
     constexpr int EB = Elem<DT>::kBytes;
     constexpr int LANES = VB / EB;
     static_assert(LANES % 4 == 0 || VB < 16, "vector lanes are moved to shared memory as float4");
+    static_assert(kThreads == 256, "the row sum adds 8 warp partials per CTA");
 
     extern __shared__ float4 row_smem[];
     float* hs = reinterpret_cast<float*>(row_smem);      // this CTA's slice of the row's fp32 h
-    __shared__ float warp_part[kThreads / 32];
-    __shared__ float slice_total[2][kMaxNormCluster];    // [row parity][cluster rank], pushed by each CTA
+    // Every warp's partial of the row's sum of squares, by row parity and
+    // cluster rank: each CTA pushes its own into every cluster peer.
+    __shared__ float wpart[2][kMaxNormCluster][kThreads / 32];
 
     const int W = P.W;
     const uint64_t H = P.hidden;
@@ -217,33 +219,33 @@ allreduce_rmsnorm_kernel(const __grid_constant__ NormParams P) {
         }
 
         // ---- the row's sum of squares, in a fixed tree ---------------------
-        // Warp shuffles, then the warp totals: this CTA's slice total, which
-        // warp 0 pushes into every cluster peer's slot for this CTA (a remote
-        // shared-memory store each; the cluster barrier's release makes them
-        // visible).  After the barrier every thread adds the C local slots in
-        // cluster-rank order, so every CTA -- and every run -- gets the same
-        // sum, with no remote read after the barrier.  The slots alternate by
-        // row parity, so a fast CTA's next row cannot overwrite a slot a peer
-        // is still reading: it would first need that peer at the next row's
-        // barrier.
+        // Warp shuffles give each warp's partial, which the warp pushes into
+        // every cluster peer's slot for (this CTA, this warp): a shared-memory
+        // store each, remote but for the CTA itself; the cluster barrier's
+        // release makes them visible.  After the barrier every thread adds,
+        // from its own CTA's copies, each CTA's 8 warp partials in one fixed
+        // tree, ((w0 + w4) + (w2 + w6)) + ((w1 + w5) + (w3 + w7)), then the C
+        // slice totals in cluster-rank order: every CTA -- and every run --
+        // gets the same sum, with no remote read and no second barrier.  The
+        // slots alternate by row parity, so a fast CTA's next row cannot
+        // overwrite a slot a peer is still reading: it would first need that
+        // peer at the next row's barrier.
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1) ss = __fadd_rn(ss, __shfl_down_sync(0xffffffffu, ss, o));
-        if (lane == 0) warp_part[warp] = ss;
-        __syncthreads();
-        if (warp == 0) {
-            float t = lane < kThreads / 32 ? warp_part[lane] : 0.0f;
-#pragma unroll
-            for (int o = 16; o > 0; o >>= 1) t = __fadd_rn(t, __shfl_down_sync(0xffffffffu, t, o));
-            t = __shfl_sync(0xffffffffu, t, 0);
-            if (lane < C) {
-                if (C == 1) slice_total[parity][0] = t;
-                else *cluster.map_shared_rank(&slice_total[parity][crank], lane) = t;
-            }
+        ss = __shfl_sync(0xffffffffu, ss, 0);
+        if (lane < C) {
+            if (C == 1) wpart[parity][0][warp] = ss;
+            else *cluster.map_shared_rank(&wpart[parity][crank][warp], lane) = ss;
         }
         if (C > 1) cluster.sync();
         else __syncthreads();
         float row_ss = 0.0f;
-        for (int r = 0; r < C; ++r) row_ss = __fadd_rn(row_ss, slice_total[parity][r]);
+        for (int r = 0; r < C; ++r) {
+            const float* q = wpart[parity][r];
+            const float t = __fadd_rn(__fadd_rn(__fadd_rn(q[0], q[4]), __fadd_rn(q[2], q[6])),
+                                      __fadd_rn(__fadd_rn(q[1], q[5]), __fadd_rn(q[3], q[7])));
+            row_ss = __fadd_rn(row_ss, t);
+        }
         const float inv = __fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(__fdiv_rn(row_ss, (float)H), P.eps)));
 
         // ---- pass 2 -------------------------------------------------------
