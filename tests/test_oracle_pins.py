@@ -429,3 +429,67 @@ def test_rejects_bad_arguments(oracle_mod):
     assert lib.or_allreduce(3, 0, 0, 2, 4, None, None) == -1
     assert lib.or_allreduce(0, 5, 0, 2, 4, None, None) == -1
     assert lib.or_allreduce(0, 0, 2, 2, 4, None, None) == -1
+
+
+def _host_reduce_one(oracle_mod, dtype, op, algo, W, N, e, y):
+    """Element e of an N-element all-reduce recomputed plainly on the host:
+    the chunk from floor(k*N/W) in Python integers, the ring order k+1, ...,
+    k or the oracle's tree (tree 1 below floor(N/2), tree 2 from there), and
+    the fold in numpy fp32 or wrapping 32-bit integers."""
+    k = max(j for j in range(W) if (j * N) // W <= e)
+    if dtype == "int32":
+        vals = [int(v) & 0xFFFFFFFF for v in y]
+        comb = {"sum": lambda a, b: (a + b) & 0xFFFFFFFF, "avg": lambda a, b: (a + b) & 0xFFFFFFFF,
+                "max": lambda a, b: b if _s32(b) > _s32(a) else a}[op]
+    else:
+        vals = [np.float32(v) for v in y]
+        if op == "avg":
+            vals = [np.float32(v * np.float32(1.0 / W)) for v in vals]
+        comb = {"sum": lambda a, b: np.float32(a + b), "avg": lambda a, b: np.float32(a + b)}[op]
+    if algo == "ring":
+        order = [(k + 1 + i) % W for i in range(W)]
+        acc = vals[order[0]]
+        for r in order[1:]:
+            acc = comb(acc, vals[r])
+    else:
+        root, _, kids = oracle_mod.tree(W, 1 if e < N // 2 else 2)
+
+        def sub(v):
+            a = vals[v]
+            for c in kids[v]:
+                a = comb(a, sub(c))
+            return a
+        acc = sub(root)
+    if dtype == "int32":
+        acc = _s32(acc)
+        if op == "avg":
+            acc = int(acc / W)          # one truncating divide of the wrapped sum
+        return np.int32(acc)
+    return np.float32(acc)
+
+
+def _s32(u):
+    return u - (1 << 32) if u & 0x80000000 else u
+
+
+@pytest.mark.parametrize("N", [2**31 + 9, 2**40 + 3, 2**62 + 5])
+@pytest.mark.parametrize("W", [2, 4, 7])
+@pytest.mark.parametrize("algo", ["ring", "tree"])
+def test_reduce_one_at_large_n(oracle_mod, N, W, algo):
+    """or_reduce_one (the oracle's one-position reduction behind the GPU's
+    checks past 2^31 elements) at positions on both sides of every chunk
+    bound and of the tree split, for N far beyond what can be allocated."""
+    rng = np.random.default_rng(N % 1000 + W)
+    es = {0, N - 1, N // 2 - 1, N // 2, N // 2 + 1}
+    for kk in range(1, W):
+        lo = (kk * N) // W
+        es |= {lo - 1, lo, lo + 1}
+    es |= {int(x) for x in rng.integers(0, N, size=5, dtype=np.uint64)}
+    for e in sorted(es):
+        yf = rng.standard_normal(W).astype(np.float32)
+        yi = rng.integers(-2**31, 2**31, size=W, dtype=np.int64).astype(np.int32)
+        for dtype, op, y in (("fp32", "sum", yf), ("fp32", "avg", yf), ("int32", "sum", yi), ("int32", "max", yi),
+                             ("int32", "avg", yi)):
+            got = oracle_mod.reduce_one(dtype, op, algo, N, e, y)
+            want = _host_reduce_one(oracle_mod, dtype, op, algo, W, N, e, y)
+            assert np.array(got).tobytes() == np.array(want).tobytes(), (dtype, op, e)
