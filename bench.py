@@ -368,11 +368,9 @@ def capture(fn, n):
     return g
 
 
-def graph_us(fn, n=50, reps=5):
-    """Device time per call (us) of a CUDA graph of n calls, best of reps replays."""
+def replay_us(g, n, reps=1):
+    """Device time per call (us) of a captured graph of n calls, best of reps replays."""
     import torch
-    g = capture(fn, n)
-    g.replay()
     best = float("inf")
     for _ in range(reps):
         a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
@@ -382,8 +380,16 @@ def graph_us(fn, n=50, reps=5):
         b.record()
         torch.cuda.synchronize()
         best = min(best, a.elapsed_time(b) * 1e3 / n)
-    del g
     return best
+
+
+def graph_us(fn, n=50, reps=5):
+    """Device time per call (us) of a CUDA graph of n calls, best of reps replays."""
+    g = capture(fn, n)
+    g.replay()
+    t = replay_us(g, n, reps)
+    del g
+    return t
 
 
 def cold_l2_us(fn, flush, n=20):
@@ -507,18 +513,31 @@ def extras(mr, torch, dev):
         row = {"N_per_rank": N, "bytes_per_rank": N * 4, "bytes_per_call": by}
         row["auto_picks"] = mr.mr_plan_auto(W, N, "fp32")[0]
         n = 200 if by <= (64 << 20) else 20
-        for algo in ("ring", "tree", "auto"):
-            def call():
-                mr.mr_allreduce(xs, ys, op="sum", algo=algo)
+        calls = {algo: (lambda a=algo: mr.mr_allreduce(xs, ys, op="sum", algo=a)) for algo in ("ring", "tree", "auto")}
+        for call in calls.values():
             for _ in range(5):
                 call()
-            t = back_to_back_us(call, n)
+        # The three are timed in turn, five rounds, each keeping its best:
+        # ring and tree often differ by less than the drift between one
+        # timing and the next, so none is timed in one block after the other.
+        b2b = {a: [] for a in calls}
+        gr = {a: [] for a in calls}
+        graphs = {a: capture(c, 50) for a, c in calls.items()} if by < GRAPH_BELOW_BYTES else {}
+        for _ in range(5):
+            for algo, call in calls.items():
+                b2b[algo].append(back_to_back_us(call, n, reps=1))
+                if algo in graphs:
+                    gr[algo].append(replay_us(graphs[algo], 50))
+        for algo, call in calls.items():
+            t = min(b2b[algo])
             row[f"{algo}_us"] = t
             row[f"{algo}_gbs"] = by / (t * 1e-6) / 1e9
-            if by < GRAPH_BELOW_BYTES:
-                t = graph_us(call, 50)
+            if algo in graphs:
+                t = min(gr[algo])
                 row[f"{algo}_graph_us"] = t
                 row[f"{algo}_graph_gbs"] = by / (t * 1e-6) / 1e9
+        graphs.clear()
+        for algo, call in calls.items():
             if by < 4 * L2_BYTES:
                 t = cold_l2_us(call, flush)
                 row[f"{algo}_cold_l2_us"] = t
@@ -531,12 +550,16 @@ def extras(mr, torch, dev):
         fastest = min(("ring", "tree"), key=lambda a: row[f"{a}_us"])
         row["auto_is_fastest"] = row["auto_picks"] == fastest
         row["auto_vs_fastest"] = row["auto_us"] / row[f"{fastest}_us"]
+        if "auto_graph_us" in row:
+            fastest = min(("ring", "tree"), key=lambda a: row[f"{a}_graph_us"])
+            row["auto_vs_fastest_graph"] = row["auto_graph_us"] / row[f"{fastest}_graph_us"]
         sweep.append(row)
         del xs, ys
     out["sweep_fp32_w8_sum"] = {
         "timing": ("us per call: back to back on one stream, one event pair around 200 calls (20 above 64 MiB); "
-                   "graph: a CUDA graph of 50 calls; cold_l2: L2 flushed before every call (graph of flush+call "
-                   "minus graph of flushes); working sets below 4x L2 are otherwise warm"),
+                   "graph: a CUDA graph of 50 calls; ring, tree and auto timed in turn over five rounds, best of "
+                   "each; cold_l2: L2 flushed before every call (graph of flush+call minus graph of flushes); "
+                   "working sets below 4x L2 are otherwise warm"),
         "rows": sweep}
 
     # FSDP: reduce-scatter avg of bf16 gradients, all-gather of bf16 parameter shards

@@ -42,16 +42,20 @@ mr_status_t fail(mr_status_t st, const char* fmt, ...) {
 size_t elem_bytes(mr_dtype_t dt) { return dt == MR_BF16 ? 2u : 4u; }
 
 // The alpha-beta cost model of the orders (t = alpha + bytes / beta), fitted
-// on GB300 per element type, rank count and order.
-struct CostRow {
-    int dtype, W, algo;
+// on GB300 per element type, rank count and order, and per range of a call's
+// buffers: latency-bound, L2-resident, streaming from HBM (as NCCL keeps one
+// (lat, bw) pair per protocol, each serving its own range of sizes).
+struct CostPair {
     double alpha_us, beta_gbs;
 };
-const CostRow kCostModel[] = {
-#include "cost_model.inc"
+struct CostRow {
+    int dtype, W, algo;
+    CostPair range[3];   // latency, L2, HBM
 };
+// kCostModelLatencyBytes, kCostModelL2Bytes and kCostModel[].
+#include "cost_model.inc"
 
-double model_us(mr_dtype_t dtype, int W, mr_algo_t algo, double bytes) {
+double model_us(mr_dtype_t dtype, int W, mr_algo_t algo, double bytes, double footprint) {
     // the row of the smallest tabulated W that covers W, else of the largest
     const CostRow* row = nullptr;
     const CostRow* largest = nullptr;
@@ -62,13 +66,16 @@ double model_us(mr_dtype_t dtype, int W, mr_algo_t algo, double bytes) {
     }
     if (!row) row = largest;
     if (!row) return 1e30;
-    return row->alpha_us + bytes / (row->beta_gbs * 1e3);
+    const CostPair& p = row->range[footprint <= kCostModelLatencyBytes ? 0 : footprint <= kCostModelL2Bytes ? 1 : 2];
+    return p.alpha_us + bytes / (p.beta_gbs * 1e3);
 }
 
 // MR_AUTO: the order with the smaller modelled time (ring on a tie).
 mr_algo_t resolve_auto(mr_dtype_t dtype, int W, size_t N, bool rs, double* predicted) {
     const double b = (double)elem_bytes(dtype) * (double)N * (rs ? (double)(W + 1) : 2.0 * W);
-    const double tr = model_us(dtype, W, MR_RING, b), tt = model_us(dtype, W, MR_TREE, b);
+    // the buffers the call touches: W inputs, and W outputs of N (all-reduce) or N/W (reduce-scatter)
+    const double footprint = (double)elem_bytes(dtype) * (double)N * (rs ? (double)(W + 1) : 2.0 * W);
+    const double tr = model_us(dtype, W, MR_RING, b, footprint), tt = model_us(dtype, W, MR_TREE, b, footprint);
     if (predicted) *predicted = tt < tr ? tt : tr;
     return tt < tr ? MR_TREE : MR_RING;
 }

@@ -212,26 +212,35 @@ def test_launch_floor_arguments(mr):
 
 
 def _cost_table():
-    rows = []
+    """(latency bound, L2 bytes, rows) of the table the library is built with;
+    a row is (dtype, W, algo, [(alpha, beta) x 3])."""
+    rows, bounds = [], {}
     path = os.path.join(ROOT, "collective_reduction_math_gb300", "csrc", "cost_model.inc")
     for line in open(path):
         line = line.strip()
-        if line.startswith("{"):
-            d, w, a, alpha, beta = [x.strip() for x in line.strip("{},").split(",")]
-            rows.append((int(d), int(w), int(a), float(alpha), float(beta)))
-    return rows
+        if line.startswith("constexpr double"):
+            name, val = line[len("constexpr double"):].split("=")
+            bounds[name.strip()] = float(val.strip(" ;"))
+        if line.startswith("{") and not line.startswith("{dtype"):
+            nums = [float(x) for x in re.findall(r"-?\d+(?:\.\d+)?", line)]
+            rows.append((int(nums[0]), int(nums[1]), int(nums[2]),
+                         [(nums[3 + 2 * i], nums[4 + 2 * i]) for i in range(3)]))
+    return bounds["kCostModelLatencyBytes"], bounds["kCostModelL2Bytes"], rows
 
 
 def test_auto_is_the_cost_model_argmin(mr):
     """MR_AUTO picks, per call, the order with the smaller alpha + bytes/beta
-    of the table the library was built with (recomputed here from the table)."""
-    rows = _cost_table()
+    of the table the library was built with, taking the (alpha, beta) of the
+    range the call's buffers fall in: latency-bound, within L2, beyond L2
+    (recomputed here from the table)."""
+    lat, l2, rows = _cost_table()
+    assert 0 < lat < l2
     assert len(rows) == 3 * 6 * 2
     codes = {"fp32": 0, "bf16": 1, "int32": 2}
     sizes = {"fp32": 4, "bf16": 2, "int32": 4}
     for dtype in codes:
         for W in (1, 2, 3, 8, 13, 16, 33, 64):
-            for N in (1 << 10, 1 << 16, 1 << 20, 1 << 24):
+            for N in (1 << 10, 1 << 14, 1 << 16, 1 << 20, 1 << 22, 1 << 24, 1 << 27):
                 for rs in (False, True):
                     b = sizes[dtype] * N * ((W + 1) if rs else 2 * W)
                     t = {}
@@ -239,7 +248,8 @@ def test_auto_is_the_cost_model_argmin(mr):
                         cand = [r for r in rows if r[0] == codes[dtype] and r[2] == a]
                         cover = [r for r in cand if r[1] >= W]
                         row = min(cover, key=lambda r: r[1]) if cover else max(cand, key=lambda r: r[1])
-                        t[a] = row[3] + b / (row[4] * 1e3)
+                        alpha, beta = row[3][0 if b <= lat else 1 if b <= l2 else 2]
+                        t[a] = alpha + b / (beta * 1e3)
                     want = "tree" if t[1] < t[0] else "ring"
                     algo, pred = mr.mr_plan_auto(W, N, dtype, rs)
                     assert algo == want, (dtype, W, N, rs)
