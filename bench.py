@@ -690,9 +690,11 @@ class Step:
         C = N // W
 
         if self.collective in ("allreduce_rmsnorm", "allreduce_then_rmsnorm"):
-            ins, res, wt = synth.workload_norm_operands(self.workload)
-            self.host_in = ins + [res, wt]
             H = w["hidden"]
+            if N % H:
+                raise ValueError(f"--n must hold whole rows of {H} elements")
+            ins, res, wt = synth.workload_norm_operands(self.workload, rows=N // H)
+            self.host_in = ins + [res, wt]
             # the fused call's algorithmic bytes (both forms are timed against them)
             self.bytes = (2 * W + 2) * N * b + H * b
             dins, douts = upload(torch, dev, self.host_in, self.dtype, [N] * (W + 1))
