@@ -565,7 +565,8 @@ mr_status_t mr_allreduce_rmsnorm(const void* const* send, void* const* recv, int
     // an SM: three of the 256 decode CTAs on one SM left it with half as much
     // again to load and store as the rest (per-phase timestamps, W = 8, 64 x
     // 8192 bf16: 5.97 against 5.50 us per step).
-    size_t smem = ((slice * 4 + 15) / 16) * 16;
+    const size_t buf_bytes = ((slice * 4 + 15) / 16) * 16;
+    size_t smem = buf_bytes;
     if (csize > 1) smem = std::max<size_t>(smem, kNormSpreadSmem);
     // One whole wave of resident CTAs, looping over the rows.  Residency is
     // the smaller of what the kernel's register budget allows (3 per SM up to
@@ -574,8 +575,28 @@ mr_status_t mr_allreduce_rmsnorm(const void* const* send, void* const* recv, int
     // that left a partial last wave measured up to 10 % slower on GB300
     // (W = 8 bf16, hidden 12288: 5032 against 5546 GB/s).
     const size_t reg_resident = W <= 8 ? 3 : W <= 16 ? 2 : 1;
-    const size_t smem_resident = std::max<size_t>(1, (227 * 1024) / (smem + 1024));
-    const size_t per_sm = std::min(reg_resident, smem_resident);
+    auto resident = [&](size_t bytes) {
+        return std::min(reg_resident, std::max<size_t>(1, (227 * 1024) / (bytes + 1024)));
+    };
+    size_t per_sm = resident(smem);
+    // One CTA per row with several rows each (up to 16 ranks): a second row
+    // buffer lets pass 2 of a row and pass 1 of the next share one loop.  That
+    // variant runs at 2 CTAs per SM (its launch bounds), and is taken where
+    // both buffers fit twice per SM and an element's W contributions take more
+    // than 8 bytes.  Measured on GB300, 4096 x 8192 rows (GB/s, one row loop
+    // at 3 CTAs per SM -> pipelined at 2): bf16 W = 8 5969 -> 6158, W = 5
+    // 5209 -> 5285, fp32 W = 8 6038 -> 6547, W = 3 4983 -> 5106; with 8
+    // bytes or fewer it loses or ties (bf16 W = 4 5137 -> 4891, fp32 W = 2
+    // 4354 -> 4375).
+    P.buf_f4 = (uint32_t)(buf_bytes / 16);
+    P.pipe = 0;
+    const size_t pipe_per_sm = std::min<size_t>(2, std::max<size_t>(1, (227 * 1024) / (2 * buf_bytes + 1024)));
+    if (csize == 1 && P.vec && vb == 16 && W <= 16 && (size_t)W * b > 8 && pipe_per_sm == 2 &&
+        rows > sms * pipe_per_sm) {
+        P.pipe = 1;
+        smem = 2 * buf_bytes;
+        per_sm = pipe_per_sm;
+    }
     const size_t clusters = std::min<size_t>(rows, std::max<size_t>(1, sms * per_sm / csize));
     const dim3 grid((unsigned)(clusters * csize), 1, 1);
     const cudaError_t err = mr::launch_allreduce_rmsnorm(P, dtype, algo, grid, smem, (cudaStream_t)stream);
@@ -583,7 +604,8 @@ mr_status_t mr_allreduce_rmsnorm(const void* const* send, void* const* recv, int
     g_launches.fetch_add(1, std::memory_order_relaxed);
     if (debug_level() > 0)
         fprintf(stderr, "[mr] allreduce_rmsnorm dtype=%s algo=%s W=%d rows=%zu hidden=%zu vector=%d grid=%u "
-                "cluster=%d smem=%zu\n", dtype_name(dtype), algo_name(algo), W, rows, hidden, P.vec, grid.x, csize, smem);
+                "cluster=%d smem=%zu pipelined=%d\n", dtype_name(dtype), algo_name(algo), W, rows, hidden, P.vec,
+                grid.x, csize, smem, P.pipe);
     return MR_OK;
 }
 

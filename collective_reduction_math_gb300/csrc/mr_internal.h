@@ -57,6 +57,9 @@ struct NormParams {
     int nseg;
     int vec;                    // 1: 16-byte (or the width's) vectors: pointers aligned, hidden % lanes == 0
     int csize;                  // CTAs per cluster; each takes a slice of a row's columns
+    int pipe;                   // 1: one CTA per row (csize 1), 16-byte vectors, two row buffers:
+                                //    pass 2 of a row runs in one loop with pass 1 of the CTA's next row
+    uint32_t buf_f4;            // pipe: float4s from one row buffer to the next
     float eps;
 };
 

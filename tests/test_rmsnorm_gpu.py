@@ -108,7 +108,10 @@ def run(mr, dtype, algo, W, rows, hidden, residual=True, residual_out=True, inpl
 @pytest.mark.parametrize("dtype", ["fp32", "bf16"])
 @pytest.mark.parametrize("algo", ["ring", "tree"])
 @pytest.mark.parametrize("W,rows,hidden", [(1, 3, 64), (2, 5, 100), (3, 7, 1000), (8, 33, 4096), (8, 4, 8192),
-                                           (13, 3, 2056), (16, 9, 2048), (17, 2, 96), (8, 2, 49152)])
+                                           (13, 3, 2056), (16, 9, 2048), (17, 2, 96), (8, 2, 49152),
+                                           # more rows than one wave of CTAs: a CTA takes 2-3 rows, pass 2 of
+                                           # one in the same loop as pass 1 of the next (two row buffers)
+                                           (8, 1000, 256), (3, 1001, 264), (16, 700, 512)])
 def test_parity(mr, dtype, algo, W, rows, hidden):
     run(mr, dtype, algo, W, rows, hidden, seed=W * 100 + rows)
 
@@ -120,6 +123,10 @@ def test_options(mr, dtype):
     run(mr, dtype, "ring", 8, 6, 512, residual=False, residual_out=True)
     run(mr, dtype, "tree", 8, 6, 512, inplace=True)
     run(mr, dtype, "ring", 5, 6, 512, offset=1)
+    # the same on rows enough for two or three per CTA
+    run(mr, dtype, "ring", 8, 1000, 128, residual=False, residual_out=True)
+    run(mr, dtype, "ring", 8, 1000, 128, residual=True, residual_out=False)
+    run(mr, dtype, "tree", 8, 1000, 128, inplace=True)
 
 
 def test_workloads_full(mr):
