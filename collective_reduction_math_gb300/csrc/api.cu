@@ -679,7 +679,12 @@ mr_status_t mr::run_sign_ef(const char* what, int mode, const void* const* grad,
     P.N = N;
     P.W = W;
     P.mode = mode;
-    P.nb = mr::sign_blocks(W, N);
+    // L1 blocks per rank: at most one full wave of the L1 kernel over all
+    // ranks (8 blocks of 256 threads per SM).  2048 blocks at W = 8 made 1.7
+    // waves, the last two-thirds full; one wave measured 6342 -> 6457 GB/s for
+    // the W = 8, 2^24 reduce-scatter step.  The partials are exact integer
+    // sums, so the scale does not depend on the block count.
+    P.nb = std::min<int>(mr::sign_blocks(W, N), std::max(1, sm_count() * 8 / W));
     P.avg = (float)(1.0 / (double)W);
     P.nseg = plan_segments(W, N, algo, P.seg);
     const int vb = mr::sign_vector_bytes(W);

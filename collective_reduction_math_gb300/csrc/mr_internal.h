@@ -101,7 +101,8 @@ constexpr int kL1Words = kL1Limbs + 1;
 constexpr uint64_t kSignMaxN = 1ull << 37;
 
 // L1 blocks per rank: one per 8192 elements, at most 2048 / W (so a call
-// never needs more than 2048 partials), at least one.
+// never needs more than 2048 partials), at least one.  This sizes the
+// workspace; a launch may use fewer blocks (one wave of the GPU).
 inline int sign_blocks(int W, uint64_t N) {
     const uint64_t cap = (uint64_t)(2048 / (W < 1 ? 1 : W));
     const uint64_t nb = (N + 8191) / 8192;
