@@ -137,14 +137,20 @@ constexpr int reduce_wcap(int W) { return W <= 2 ? 2 : W <= 4 ? 4 : W <= 8 ? 8 :
 constexpr bool reduce_pairs(int dtype, int op, bool hop) {
     return dtype == MR_BF16 && hop && (op == MR_SUM || op == MR_AVG);
 }
-// Above 16 ranks every order folds the ranks in batches of 8 with 16-byte
-// vectors, except the tree on bf16 lanes unpacked to fp32, which takes 8-byte
-// vectors (4 lanes) so that the per-batch partials of all 8 batches fit in
-// registers.  The host's alignment check and the kernel's template both take
-// the width from here.
+// Every variant of the reduce kernel moves 16-byte vectors; the host's
+// alignment check and the kernel's template both take the width from here.
 constexpr int reduce_vector_bytes(int W, int algo, int dtype, int op, bool hop) {
-    return (W <= 16 || algo != MR_TREE || dtype != MR_BF16 || reduce_pairs(dtype, op, hop)) ? 16 : 8;
+    (void)W; (void)algo; (void)dtype; (void)op; (void)hop;
+    return 16;
 }
+// The batched tree over 64 slots on bf16 lanes unpacked to fp32 keeps its 8
+// batches' in-batch top subtotals (8 lanes each) in shared memory, per
+// thread, instead of registers: with them in registers it needed 8-byte
+// vectors (4 lanes) to fit, and ran at 5.3-5.5 TB/s.
+constexpr bool reduce_top_shared(int wcap, int dtype, int vb, bool pairs) {
+    return wcap == 64 && dtype == MR_BF16 && vb == 16 && !pairs;
+}
+constexpr size_t reduce_top_shared_bytes(int lanes) { return (size_t)8 * lanes * kThreads * sizeof(float); }
 // The fused RMSNorm kernel keeps all W values of a lane in registers and so
 // narrows its vectors to 4 bytes above 16 ranks.
 constexpr int norm_vector_bytes(int W) { return W <= 16 ? 16 : 4; }

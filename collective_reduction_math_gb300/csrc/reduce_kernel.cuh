@@ -444,6 +444,12 @@ reduce_kernel(const __grid_constant__ ReduceParams P) {
     constexpr bool kTable = BATCH;
     constexpr bool kBatched = BATCH && ALGO != MR_TREE;
     constexpr bool kTreeBatched = BATCH && ALGO == MR_TREE;
+    // The 64-slot bf16 tree with fp32 accumulation on 16-byte vectors keeps
+    // its 8 batches' top subtotals in dynamic shared memory (see
+    // reduce_top_shared).
+    constexpr bool kTopShared = kTreeBatched && WCAP == 64 && DT == MR_BF16 && VB == 16 && !kPairs;   // reduce_top_shared()
+    extern __shared__ float dyn_smem[];
+    unit_t* const top_smem = reinterpret_cast<unit_t*>(dyn_smem);
     static_assert(!BATCH || WCAP % 8 == 0, "batches of 8 positions");
     __shared__ const char* table[kTable ? WCAP : 1];
     const char* src[kTable ? 1 : WCAP];
@@ -590,7 +596,15 @@ reduce_kernel(const __grid_constant__ ReduceParams P) {
                 if (v0 < vb) {
                     const uint64_t off = v0 * VB;
                     const int M = (W + 7) >> 3;
-                    unit_t head[NB][UNITS], top[NB][UNITS];
+                    // The batches' in-batch top subtotals are read once, when
+                    // the heads are folded; with kTopShared they wait in this
+                    // thread's own shared-memory slots ([batch][unit][thread])
+                    // rather than in registers.
+                    unit_t head[NB][UNITS], top_reg[kTopShared ? 1 : NB][kTopShared ? 1 : UNITS];
+                    auto top_at = [&](int m, int u) -> unit_t& {
+                        if constexpr (kTopShared) return top_smem[((uint64_t)m * UNITS + u) * kThreads + threadIdx.x];
+                        else return top_reg[m][u];
+                    };
 #pragma unroll
                     for (int m = 0; m < NB; ++m) {
                         if (m < M) {
@@ -606,7 +620,7 @@ reduce_kernel(const __grid_constant__ ReduceParams P) {
                                 for (int q = 0; q < 8; ++q)
                                     if (q < Wb) y[q] = unit(raw[q], u);
                                 head[m][u] = y[0];
-                                top[m][u] = utop(y, Wb);
+                                top_at(m, u) = utop(y, Wb);
                             }
                         }
                     }
@@ -617,7 +631,7 @@ reduce_kernel(const __grid_constant__ ReduceParams P) {
                             if (m < M) {
 #pragma unroll
                                 for (int u = 0; u < UNITS; ++u) {
-                                    unit_t a = ucomb(head[m][u], B == 1 ? top[m - 1][u] : head[m - B / 2][u]);
+                                    unit_t a = ucomb(head[m][u], B == 1 ? top_at(m - 1, u) : head[m - B / 2][u]);
                                     bool taken = false;
 #pragma unroll
                                     for (int h = B / 2; h >= 1; h >>= 1) {
@@ -626,7 +640,7 @@ reduce_kernel(const __grid_constant__ ReduceParams P) {
                                             taken = true;
                                         }
                                     }
-                                    if (!taken && 8 * m + 1 < W) a = ucomb(a, top[m][u]);
+                                    if (!taken && 8 * m + 1 < W) a = ucomb(a, top_at(m, u));
                                     head[m][u] = a;
                                 }
                             }
@@ -742,10 +756,17 @@ cudaError_t launch_reduce(const ReduceParams& P, int op, dim3 grid, cudaStream_t
                 if (reduce_batched(P.W, ALGO, DT, HOP))
                     return launch_kernel(reduce_kernel<DT, OP, ALGO, 16, 16, 1, HOP, true>, grid, 0, stream, 0, P);
                 return launch_kernel(reduce_kernel<DT, OP, ALGO, 16, 16, reduce_unroll_for(16, false), HOP, false>, grid, 0, stream, 0, P);
-            default:
-                return launch_kernel(reduce_kernel<DT, OP, ALGO, 64, reduce_vector_bytes(64, ALGO, DT, OP, HOP),
-                                                   reduce_unroll_for(64, false), HOP, true>,
-                                     grid, 0, stream, 0, P);
+            default: {
+                constexpr int VB = reduce_vector_bytes(64, ALGO, DT, OP, HOP);
+                auto k = reduce_kernel<DT, OP, ALGO, 64, VB, reduce_unroll_for(64, false), HOP, true>;
+                size_t smem = 0;
+                if constexpr (ALGO == MR_TREE && reduce_top_shared(64, DT, VB, reduce_pairs(DT, OP, HOP))) {
+                    smem = reduce_top_shared_bytes(VB / Elem<DT>::kBytes);
+                    const cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+                    if (e != cudaSuccess) return e;
+                }
+                return launch_kernel(k, grid, smem, stream, 0, P);
+            }
         }
     };
     switch (op) {
