@@ -240,9 +240,9 @@ int plan_segments_hier(int W, uint64_t N, int group, bool cut_at_chunks, mr::Seg
     return n;
 }
 
-dim3 plan_tiles(mr::ReduceParams& P, int lanes, bool batched) {
+dim3 plan_tiles(mr::ReduceParams& P, int algo, int lanes, bool batched, bool wide_heads) {
     const bool rs = P.mode == mr::MODE_REDUCE_SCATTER;
-    const int u = mr::reduce_unroll(P.W, rs);
+    const int u = mr::reduce_unroll(P.W, algo, rs);
     const uint64_t per_tile = P.vec ? (uint64_t)mr::kThreads * u : (uint64_t)mr::kThreads;
     P.tile_start[0] = 0;
     P.tiles_max = 0;
@@ -258,7 +258,7 @@ dim3 plan_tiles(mr::ReduceParams& P, int lanes, bool batched) {
     }
     const uint64_t vtiles = P.vec ? P.tiles_max * P.nseg : P.tile_start[P.nseg];
     const uint64_t tiles = std::max<uint64_t>(vtiles, (uint64_t)P.nseg);
-    const int per_sm = mr::reduce_blocks_per_sm(mr::reduce_wcap(P.W), u, batched);
+    const int per_sm = mr::reduce_blocks_per_sm(mr::reduce_wcap(P.W, algo), u, batched, wide_heads);
     const uint64_t gx = std::min<uint64_t>((uint64_t)sm_count() * per_sm, tiles);
     return dim3((unsigned)std::max<uint64_t>(gx, 1), 1, 1);
 }
@@ -312,7 +312,8 @@ mr_status_t run_reduce(const char* what, int mode, const void* const* send, void
         vec = vec && ((uintptr_t)send[r] % vb == 0) && ((uintptr_t)recv[r] % vb == 0);
     if (mode == mr::MODE_REDUCE_SCATTER) vec = vec && ((N / W) * eb) % vb == 0;
     P.vec = vec ? 1 : 0;
-    const dim3 grid = plan_tiles(P, vb / eb, mr::reduce_batched(W, algo, dtype, hop != 0));
+    const dim3 grid = plan_tiles(P, algo, vb / eb, mr::reduce_batched(W, algo, dtype, hop != 0),
+                                 mr::reduce_wide_heads(mr::reduce_wcap(W, algo), algo));
     const cudaError_t err = launch_reduce(dtype, P, op, algo, grid, (cudaStream_t)stream);
     if (err != cudaSuccess)
         return fail(MR_ERR_CUDA, "%s launch failed: %s", what, cudaGetErrorString(err));

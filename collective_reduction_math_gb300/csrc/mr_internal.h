@@ -132,7 +132,12 @@ struct GatherParams {
 // thread (U*W ~ 8) at 3 CTAs per SM up to W = 8.  Reduce-scatter stores one
 // vector per W loads, and at W = 8 runs faster with two vectors per thread at
 // 2 CTAs per SM (measured on GB300: 6.8 against 5.8 TB/s).
-constexpr int reduce_wcap(int W) { return W <= 2 ? 2 : W <= 4 ? 4 : W <= 8 ? 8 : W <= 16 ? 16 : 64; }
+// Above 16 ranks the tree takes 32 slots (4 batch heads) up to 32 ranks and
+// 64 (8 heads) beyond; the left folds take 64 at any W above 16 (their
+// batched fold does not depend on the slot count).
+constexpr int reduce_wcap(int W, int algo) {
+    return W <= 2 ? 2 : W <= 4 ? 4 : W <= 8 ? 8 : W <= 16 ? 16 : (algo == MR_TREE && W <= 32) ? 32 : 64;
+}
 // Per-hop bf16 sum and avg fold packed pairs (two lanes per 32-bit word).
 constexpr bool reduce_pairs(int dtype, int op, bool hop) {
     return dtype == MR_BF16 && hop && (op == MR_SUM || op == MR_AVG);
@@ -143,27 +148,32 @@ constexpr int reduce_vector_bytes(int W, int algo, int dtype, int op, bool hop) 
     (void)W; (void)algo; (void)dtype; (void)op; (void)hop;
     return 16;
 }
-// The batched tree over 64 slots on bf16 lanes unpacked to fp32 keeps its 8
-// batches' in-batch top subtotals (8 lanes each) in shared memory, per
-// thread, instead of registers: with them in registers it needed 8-byte
-// vectors (4 lanes) to fit, and ran at 5.3-5.5 TB/s.
-constexpr bool reduce_top_shared(int wcap, int dtype, int vb, bool pairs) {
-    return wcap == 64 && dtype == MR_BF16 && vb == 16 && !pairs;
+// The batched tree over 64 slots keeps its 8 batches' in-batch top subtotals
+// (one per unit: a lane, or a packed pair of bf16 lanes) in shared memory,
+// per thread, instead of registers: each is written once and read once.
+constexpr bool reduce_top_shared(int wcap, int algo) { return wcap >= 32 && algo == MR_TREE; }
+constexpr size_t reduce_top_shared_bytes(int wcap, int units) {
+    return (size_t)(wcap / 8) * units * kThreads * sizeof(uint32_t);
 }
-constexpr size_t reduce_top_shared_bytes(int lanes) { return (size_t)8 * lanes * kThreads * sizeof(float); }
+// The variants whose live state does not fit 80 registers: the 64-slot
+// batched trees (8 heads of 4 or 8 units beside a batch of 8 vectors; the
+// 32-slot tree keeps 4).
+constexpr bool reduce_wide_heads(int wcap, int algo) { return wcap == 64 && algo == MR_TREE; }
 // The fused RMSNorm kernel keeps all W values of a lane in registers and so
 // narrows its vectors to 4 bytes above 16 ranks.
 constexpr int norm_vector_bytes(int W) { return W <= 16 ? 16 : 4; }
 constexpr int reduce_unroll_for(int wcap, bool rs) {
     return wcap == 2 ? 4 : wcap == 4 ? 2 : (wcap == 8 && rs) ? 2 : 1;
 }
-constexpr int reduce_unroll(int W, bool rs) { return reduce_unroll_for(reduce_wcap(W), rs); }
+constexpr int reduce_unroll(int W, int algo, bool rs) { return reduce_unroll_for(reduce_wcap(W, algo), rs); }
 // Resident CTAs per SM (the kernel's launch bounds and the grid's size): 3 for
-// the all-reduce up to 8 ranks and for the 16-slot batched folds (8 vectors
-// live at a time), else 2.  At 2 per SM the batched W = 16 folds sat at 24 %
-// of warps active, stalled on loads (ncu, int32 W = 16: 74 % of DRAM peak).
-constexpr int reduce_blocks_per_sm(int wcap, int u, bool batch) {
-    return ((wcap <= 8 && wcap * u <= 8) || (batch && wcap == 16)) ? 3 : 2;
+// the all-reduce up to 8 ranks and for the batched folds (8 vectors live at a
+// time), except the 64-slot trees, else 2.  At 2 per SM the batched W = 16
+// folds sat at 24 % of warps active, stalled on loads (ncu, int32 W = 16: 74 %
+// of DRAM peak); above 16 ranks 3 per SM took the rings from 5.3-5.6 to
+// 6.1-6.2 TB/s at W = 17 and the 32-slot trees from 4.9-5.2 to 5.7-6.0.
+constexpr int reduce_blocks_per_sm(int wcap, int u, bool batch, bool wide_heads) {
+    return ((wcap <= 8 && wcap * u <= 8) || (batch && !wide_heads)) ? 3 : 2;
 }
 // Whether the reduce kernel for (W, order, element type, per-hop rounding)
 // folds in batches of 8: only 8 vectors and no pointers live in registers, so

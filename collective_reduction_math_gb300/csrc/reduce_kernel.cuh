@@ -217,6 +217,123 @@ __device__ __forceinline__ typename A::acc_t tree_batch_top(typename A::acc_t (&
     return Wb > 4 ? y[4] : Wb > 2 ? y[2] : y[1];
 }
 
+// The batched folds, generic over what a "unit" is (one lane's value, or a
+// packed pair of bf16 lanes) and where a batch comes from: load(m, Wb, raw)
+// loads positions [8m, 8m + Wb) into raw[0, Wb), unit(raw[q], u) is unit u of
+// one position's contribution, comb(a, b) combines two units.  The vector
+// tiles and the element-wise heads and tails run the same code.
+
+// A left fold over many positions (ring; hierarchical when HIER, gmask
+// marking where each group starts): the positions come in batches of 8 and
+// the fold's state -- the running group part and the total of the groups so
+// far -- carries from batch to batch.  Same order, same operations as the
+// position-by-position fold.
+template <bool HIER, int UNITS, class T, class R, class Load, class Unit, class Comb>
+__device__ __forceinline__ void batched_left_fold(int W, uint64_t gmask, Load load, Unit unit, Comb comb,
+                                                  T (&part)[UNITS]) {
+    T total[UNITS];
+    bool have_total = false;
+    for (int b0 = 0; b0 < W; b0 += 8) {
+        R raw[8];
+        load(b0 >> 3, min(8, W - b0), raw);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            const int p = b0 + i;
+            if (p >= W) break;
+            if (p == 0) {
+#pragma unroll
+                for (int u = 0; u < UNITS; ++u) part[u] = unit(raw[i], u);
+            } else if (HIER && ((gmask >> p) & 1u)) {
+                if (have_total) {
+#pragma unroll
+                    for (int u = 0; u < UNITS; ++u) total[u] = comb(total[u], part[u]);
+                } else {
+#pragma unroll
+                    for (int u = 0; u < UNITS; ++u) total[u] = part[u];
+                }
+                have_total = true;
+#pragma unroll
+                for (int u = 0; u < UNITS; ++u) part[u] = unit(raw[i], u);
+            } else {
+#pragma unroll
+                for (int u = 0; u < UNITS; ++u) part[u] = comb(part[u], unit(raw[i], u));
+            }
+        }
+    }
+    if (have_total) {
+#pragma unroll
+        for (int u = 0; u < UNITS; ++u) part[u] = comb(total[u], part[u]);
+    }
+}
+
+// The tree order over many positions: each batch of 8 positions is loaded and
+// folded up to its in-batch top node (top, i.e. tree_batch_top), keeping per
+// batch only the head's own value and that subtotal (top_at(m, u): where
+// batch m's top of unit u waits).  The heads 8m then form the same bit-trick
+// tree over m (level = lowest set bit of m): a head takes its own value, then
+// its lower child (the previous batch's top for m odd, else head m - B/2),
+// then its upper child (head m + h for the largest h in {B/2, ..., 1} below
+// the number of heads, else its own batch's top).  The root takes its one
+// child.  These are fold_tree's combines in fold_tree's order.
+template <int NB, int UNITS, class T, class R, class Load, class Unit, class Comb, class Top, class TopAt>
+__device__ __forceinline__ void batched_tree(int W, Load load, Unit unit, Comb comb, Top top, TopAt top_at,
+                                             T (&root)[UNITS]) {
+    const int M = (W + 7) >> 3;
+    T head[NB][UNITS];
+#pragma unroll
+    for (int m = 0; m < NB; ++m) {
+        if (m < M) {
+            const int Wb = min(8, W - 8 * m);
+            R raw[8];
+            load(m, Wb, raw);
+#pragma unroll
+            for (int u = 0; u < UNITS; ++u) {
+                T y[8];
+#pragma unroll
+                for (int q = 0; q < 8; ++q)
+                    if (q < Wb) y[q] = unit(raw[q], u);
+                head[m][u] = y[0];
+                top_at(m, u) = top(y, Wb);
+            }
+        }
+    }
+#pragma unroll
+    for (int B = 1; B < NB; B <<= 1) {
+#pragma unroll
+        for (int m = B; m < NB; m += 2 * B) {
+            if (m < M) {
+#pragma unroll
+                for (int u = 0; u < UNITS; ++u) {
+                    T a = comb(head[m][u], B == 1 ? top_at(m - 1, u) : head[m - B / 2][u]);
+                    bool taken = false;
+#pragma unroll
+                    for (int h = B / 2; h >= 1; h >>= 1) {
+                        if (!taken && m + h < M) {
+                            a = comb(a, head[m + h][u]);
+                            taken = true;
+                        }
+                    }
+                    if (!taken && 8 * m + 1 < W) a = comb(a, top_at(m, u));
+                    head[m][u] = a;
+                }
+            }
+        }
+    }
+#pragma unroll
+    for (int u = 0; u < UNITS; ++u) {
+        T a = head[0][u];
+        bool taken = false;
+#pragma unroll
+        for (int h = NB / 2; h >= 1; h >>= 1) {
+            if (!taken && h < M) {
+                a = comb(a, head[h][u]);
+                taken = true;
+            }
+        }
+        root[u] = a;
+    }
+}
+
 // Hierarchical: positions come group by group (gmask marks the first position
 // of each group); each group's positions are folded left to right, then the
 // group totals left to right.
@@ -374,7 +491,7 @@ __device__ __forceinline__ int order_rank(int W, const Segment& sg, int i, int g
 }
 
 template <int DT, int OP, int ALGO, int WCAP, int VB, int U, bool HOP, bool BATCH>
-__global__ void __launch_bounds__(kThreads, reduce_blocks_per_sm(WCAP, U, BATCH))
+__global__ void __launch_bounds__(kThreads, reduce_blocks_per_sm(WCAP, U, BATCH, reduce_wide_heads(WCAP, ALGO)))
 reduce_kernel(const __grid_constant__ ReduceParams P) {
     using A = Arith<DT, OP>;
     using raw_t = typename A::raw_t;
@@ -442,25 +559,38 @@ reduce_kernel(const __grid_constant__ ReduceParams P) {
     // one (BATCH: the ranks are loaded and folded in batches of 8, so only 8
     // vectors are live at a time).
     constexpr bool kTable = BATCH;
-    constexpr bool kBatched = BATCH && ALGO != MR_TREE;
     constexpr bool kTreeBatched = BATCH && ALGO == MR_TREE;
-    // The 64-slot bf16 tree with fp32 accumulation on 16-byte vectors keeps
-    // its 8 batches' top subtotals in dynamic shared memory (see
-    // reduce_top_shared).
-    constexpr bool kTopShared = kTreeBatched && WCAP == 64 && DT == MR_BF16 && VB == 16 && !kPairs;   // reduce_top_shared()
+    // The 32- and 64-slot trees keep their batches' top subtotals in dynamic
+    // shared memory (see reduce_top_shared).
+    constexpr bool kTopShared = kTreeBatched && WCAP >= 32;   // reduce_top_shared()
     extern __shared__ float dyn_smem[];
     unit_t* const top_smem = reinterpret_cast<unit_t*>(dyn_smem);
     static_assert(!BATCH || WCAP % 8 == 0, "batches of 8 positions");
-    __shared__ const char* table[kTable ? WCAP : 1];
+    // The 64-slot trees (2 CTAs per SM) keep one table per warp: a warp that
+    // moves to another segment rewrites its own copy between two warp
+    // barriers while the CTA's other warps run on.  The other batched folds
+    // (3 CTAs per SM) share one table per CTA: there the CTA-wide barrier
+    // measured faster (warps that stay on one tile together, 3-6 % at 10-28
+    // ranks), at 2 CTAs per SM slower (the 64-slot trees 4-12 %), except for
+    // bf16 min and max (2-5 % faster with the CTA's table at 57 and 64 ranks).
+    constexpr bool kWarpTable = kTable && WCAP == 64 && ALGO == MR_TREE && !(DT == MR_BF16 && A::kKeyed);
+    constexpr int kTables = kWarpTable ? kThreads / 32 : 1;
+    __shared__ const char* table[kTables][kTable ? WCAP : 1];
     const char* src[kTable ? 1 : WCAP];
     int cur = -1;
     auto enter = [&](int seg) {
         if (seg == cur) return;
         cur = seg;
-        if constexpr (kTable) {
+        if constexpr (kWarpTable) {
+            const int wp = threadIdx.x >> 5;
+            __syncwarp();
+            for (int i = threadIdx.x & 31; i < W; i += 32)
+                table[wp][i] = static_cast<const char*>(P.in[order_rank<ALGO>(W, P.seg[seg], i, P.group)]);
+            __syncwarp();
+        } else if constexpr (kTable) {
             __syncthreads();
             if (threadIdx.x < W)
-                table[threadIdx.x] = static_cast<const char*>(P.in[order_rank<ALGO>(W, P.seg[seg], threadIdx.x, P.group)]);
+                table[0][threadIdx.x] = static_cast<const char*>(P.in[order_rank<ALGO>(W, P.seg[seg], threadIdx.x, P.group)]);
             __syncthreads();
         } else {
 #pragma unroll
@@ -469,23 +599,45 @@ reduce_kernel(const __grid_constant__ ReduceParams P) {
         }
     };
     auto input = [&](int i) -> const char* {
-        if constexpr (kTable) return table[i];
+        if constexpr (kWarpTable) return table[threadIdx.x >> 5][i];
+        else if constexpr (kTable) return table[0][i];
         else return src[i];
     };
 
-    // One element, reduced from scratch (heads, tails, unaligned buffers).
+    // One element, reduced from scratch (heads, tails, unaligned buffers);
+    // the batched kernels fold it in batches as their vector tiles do.
     auto element = [&](const Segment& sg, uint64_t e) {
-        acc_t y[WCAP];
+        raw_t r;
+        if constexpr (BATCH) {
+            auto load = [&](int m, int Wb, raw_t (&raw)[8]) {
 #pragma unroll
-        for (int i = 0; i < WCAP; ++i)
-            if (i < W) y[i] = contrib(__ldg(reinterpret_cast<const raw_t*>(input(i)) + e));
-        const raw_t r = A::post(fold<A, ALGO, WCAP>(y, W, hop, gmask), W);
+                for (int q = 0; q < 8; ++q)
+                    if (q < Wb) raw[q] = __ldg(reinterpret_cast<const raw_t*>(input(8 * m + q)) + e);
+            };
+            auto one = [&](raw_t x, int) -> acc_t { return contrib(x); };
+            auto cb = [&](acc_t a, acc_t b) -> acc_t { return comb<A>(a, b, hop); };
+            acc_t res[1];
+            if constexpr (ALGO == MR_TREE) {
+                acc_t tops[WCAP / 8];
+                batched_tree<WCAP / 8, 1, acc_t, raw_t>(
+                    W, load, one, cb, [&](acc_t (&y)[8], int Wb) -> acc_t { return tree_batch_top<A>(y, Wb, hop); },
+                    [&](int m, int) -> acc_t& { return tops[m]; }, res);
+            } else {
+                batched_left_fold<ALGO == MR_HIER, 1, acc_t, raw_t>(W, gmask, load, one, cb, res);
+            }
+            r = A::post(res[0], W);
+        } else {
+            acc_t y[WCAP];
+#pragma unroll
+            for (int i = 0; i < WCAP; ++i)
+                if (i < W) y[i] = contrib(__ldg(reinterpret_cast<const raw_t*>(input(i)) + e));
+            r = A::post(fold<A, ALGO, WCAP>(y, W, hop, gmask), W);
+        }
         if (rs) {
             static_cast<raw_t*>(P.out[sg.k])[e - sg.out_lo] = r;
         } else {
-#pragma unroll
-            for (int j = 0; j < WCAP; ++j)
-                if (j < W) static_cast<raw_t*>(P.out[j])[e] = r;
+#pragma unroll 8
+            for (int j = 0; j < W; ++j) static_cast<raw_t*>(P.out[j])[e] = r;
         }
     };
 
@@ -524,144 +676,35 @@ reduce_kernel(const __grid_constant__ ReduceParams P) {
             const Segment& sg = P.seg[seg];
             const uint64_t va = (sg.lo + LANES - 1) / LANES, vb = sg.hi / LANES;
             const uint64_t v0 = va + local * kTile + threadIdx.x;
-            if constexpr (kBatched) {
-                // A left-fold order (ring, hierarchical) over many ranks:
-                // the ranks come in batches of 8 (8 independent 16-byte loads
-                // in flight, as at W = 8) and the fold's state -- the running
-                // group part and the total of the groups so far -- carries
-                // from batch to batch.  Same order, same operations.
+            if constexpr (BATCH) {
+                // Many ranks: the positions are loaded and folded in batches
+                // of 8 (8 independent 16-byte loads in flight, as at W = 8).
                 static_assert(U == 1, "the batched folds take one vector per thread per tile");
                 if (v0 < vb) {
                     const uint64_t off = v0 * VB;
-                    unit_t part[UNITS], total[UNITS];
-                    bool have_total = false;
-                    for (int b0 = 0; b0 < W; b0 += 8) {
-                        Vec<VB> raw[8];
+                    auto load = [&](int m, int Wb, Vec<VB> (&raw)[8]) {
 #pragma unroll
-                        for (int i = 0; i < 8; ++i)
-                            if (b0 + i < W) raw[i] = load_vec<VB>(input(b0 + i) + off);
-#pragma unroll
-                        for (int i = 0; i < 8; ++i) {
-                            const int p = b0 + i;
-                            if (p >= W) break;
-                            if (p == 0) {
-#pragma unroll
-                                for (int u = 0; u < UNITS; ++u) part[u] = unit(raw[i], u);
-                            } else if (ALGO == MR_HIER && ((gmask >> p) & 1u)) {
-                                if (have_total) {
-#pragma unroll
-                                    for (int u = 0; u < UNITS; ++u) total[u] = ucomb(total[u], part[u]);
-                                } else {
-#pragma unroll
-                                    for (int u = 0; u < UNITS; ++u) total[u] = part[u];
-                                }
-                                have_total = true;
-#pragma unroll
-                                for (int u = 0; u < UNITS; ++u) part[u] = unit(raw[i], u);
-                            } else {
-#pragma unroll
-                                for (int u = 0; u < UNITS; ++u) part[u] = ucomb(part[u], unit(raw[i], u));
-                            }
-                        }
-                    }
-                    if (have_total) {
-#pragma unroll
-                        for (int u = 0; u < UNITS; ++u) part[u] = ucomb(total[u], part[u]);
-                    }
-                    Vec<VB> res;
-                    upost(part, res);
-                    if (rs) {
-                        store_vec<VB>(static_cast<char*>(P.out[sg.k]) + off - sg.out_lo * EB, res);
-                    } else {
-#pragma unroll 8
-                        for (int j = 0; j < W; ++j) store_vec<VB>(static_cast<char*>(P.out[j]) + off, res);
-                    }
-                }
-                continue;
-            }
-            if constexpr (kTreeBatched) {
-                // The tree order over many ranks: each batch of 8
-                // positions is loaded (8 vectors in flight) and folded up to
-                // its in-batch top node (tree_batch_top), keeping per batch
-                // only the head's own value and that subtotal.  The heads 8m
-                // then form the same bit-trick tree over m (level = lowest set
-                // bit of m): a head takes its own value, then its lower child
-                // (the previous batch's top for m odd, else head m - B/2), then
-                // its upper child (head m + h for the largest h in {B/2, ..., 1}
-                // below the number of heads, else its own batch's top).  The
-                // root takes its one child.  These are fold_tree's combines in
-                // fold_tree's order.
-                static_assert(U == 1, "the batched folds take one vector per thread per tile");
-                constexpr int NB = WCAP / 8;      // batches of 8 positions
-                if (v0 < vb) {
-                    const uint64_t off = v0 * VB;
-                    const int M = (W + 7) >> 3;
-                    // The batches' in-batch top subtotals are read once, when
-                    // the heads are folded; with kTopShared they wait in this
-                    // thread's own shared-memory slots ([batch][unit][thread])
-                    // rather than in registers.
-                    unit_t head[NB][UNITS], top_reg[kTopShared ? 1 : NB][kTopShared ? 1 : UNITS];
-                    auto top_at = [&](int m, int u) -> unit_t& {
-                        if constexpr (kTopShared) return top_smem[((uint64_t)m * UNITS + u) * kThreads + threadIdx.x];
-                        else return top_reg[m][u];
+                        for (int q = 0; q < 8; ++q)
+                            if (q < Wb) raw[q] = load_vec<VB>(input(8 * m + q) + off);
                     };
-#pragma unroll
-                    for (int m = 0; m < NB; ++m) {
-                        if (m < M) {
-                            const int Wb = min(8, W - 8 * m);
-                            Vec<VB> raw[8];
-#pragma unroll
-                            for (int q = 0; q < 8; ++q)
-                                if (q < Wb) raw[q] = load_vec<VB>(input(8 * m + q) + off);
-#pragma unroll
-                            for (int u = 0; u < UNITS; ++u) {
-                                unit_t y[8];
-#pragma unroll
-                                for (int q = 0; q < 8; ++q)
-                                    if (q < Wb) y[q] = unit(raw[q], u);
-                                head[m][u] = y[0];
-                                top_at(m, u) = utop(y, Wb);
-                            }
-                        }
-                    }
-#pragma unroll
-                    for (int B = 1; B < NB; B <<= 1) {
-#pragma unroll
-                        for (int m = B; m < NB; m += 2 * B) {
-                            if (m < M) {
-#pragma unroll
-                                for (int u = 0; u < UNITS; ++u) {
-                                    unit_t a = ucomb(head[m][u], B == 1 ? top_at(m - 1, u) : head[m - B / 2][u]);
-                                    bool taken = false;
-#pragma unroll
-                                    for (int h = B / 2; h >= 1; h >>= 1) {
-                                        if (!taken && m + h < M) {
-                                            a = ucomb(a, head[m + h][u]);
-                                            taken = true;
-                                        }
-                                    }
-                                    if (!taken && 8 * m + 1 < W) a = ucomb(a, top_at(m, u));
-                                    head[m][u] = a;
-                                }
-                            }
-                        }
-                    }
-                    unit_t root[UNITS];
-#pragma unroll
-                    for (int u = 0; u < UNITS; ++u) {
-                        unit_t a = head[0][u];
-                        bool taken = false;
-#pragma unroll
-                        for (int h = NB / 2; h >= 1; h >>= 1) {
-                            if (!taken && h < M) {
-                                a = ucomb(a, head[h][u]);
-                                taken = true;
-                            }
-                        }
-                        root[u] = a;
+                    unit_t res_u[UNITS];
+                    if constexpr (kTreeBatched) {
+                        // The batches' in-batch top subtotals are read once,
+                        // when the heads are folded; with kTopShared they wait
+                        // in this thread's own shared-memory slots
+                        // ([batch][unit][thread]) rather than in registers.
+                        constexpr int NB = WCAP / 8;
+                        unit_t top_reg[kTopShared ? 1 : NB][kTopShared ? 1 : UNITS];
+                        auto top_at = [&](int m, int u) -> unit_t& {
+                            if constexpr (kTopShared) return top_smem[((uint64_t)m * UNITS + u) * kThreads + threadIdx.x];
+                            else return top_reg[m][u];
+                        };
+                        batched_tree<NB, UNITS, unit_t, Vec<VB>>(W, load, unit, ucomb, utop, top_at, res_u);
+                    } else {
+                        batched_left_fold<ALGO == MR_HIER, UNITS, unit_t, Vec<VB>>(W, gmask, load, unit, ucomb, res_u);
                     }
                     Vec<VB> res;
-                    upost(root, res);
+                    upost(res_u, res);
                     if (rs) {
                         store_vec<VB>(static_cast<char*>(P.out[sg.k]) + off - sg.out_lo * EB, res);
                     } else {
@@ -746,7 +789,21 @@ cudaError_t launch_reduce(const ReduceParams& P, int op, dim3 grid, cudaStream_t
     auto go = [&](auto op_c) -> cudaError_t {
         constexpr int OP = decltype(op_c)::value;
         const bool rs = P.mode == MODE_REDUCE_SCATTER;
-        switch (reduce_wcap(P.W)) {
+        // The batched kernels above 16 ranks; the trees' top subtotals take
+        // dynamic shared memory.
+        auto launch_wide = [&](auto wc) -> cudaError_t {
+            constexpr int WC = decltype(wc)::value;
+            constexpr int VB = reduce_vector_bytes(WC, ALGO, DT, OP, HOP);
+            auto k = reduce_kernel<DT, OP, ALGO, WC, VB, reduce_unroll_for(WC, false), HOP, true>;
+            size_t smem = 0;
+            if constexpr (reduce_top_shared(WC, ALGO)) {
+                smem = reduce_top_shared_bytes(WC, reduce_pairs(DT, OP, HOP) ? VB / 4 : VB / Elem<DT>::kBytes);
+                const cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+                if (e != cudaSuccess) return e;
+            }
+            return launch_kernel(k, grid, smem, stream, 0, P);
+        };
+        switch (reduce_wcap(P.W, ALGO)) {
             case 2: return launch_kernel(reduce_kernel<DT, OP, ALGO, 2, 16, reduce_unroll_for(2, false), HOP, false>, grid, 0, stream, 0, P);
             case 4: return launch_kernel(reduce_kernel<DT, OP, ALGO, 4, 16, reduce_unroll_for(4, false), HOP, false>, grid, 0, stream, 0, P);
             case 8:
@@ -756,17 +813,11 @@ cudaError_t launch_reduce(const ReduceParams& P, int op, dim3 grid, cudaStream_t
                 if (reduce_batched(P.W, ALGO, DT, HOP))
                     return launch_kernel(reduce_kernel<DT, OP, ALGO, 16, 16, 1, HOP, true>, grid, 0, stream, 0, P);
                 return launch_kernel(reduce_kernel<DT, OP, ALGO, 16, 16, reduce_unroll_for(16, false), HOP, false>, grid, 0, stream, 0, P);
-            default: {
-                constexpr int VB = reduce_vector_bytes(64, ALGO, DT, OP, HOP);
-                auto k = reduce_kernel<DT, OP, ALGO, 64, VB, reduce_unroll_for(64, false), HOP, true>;
-                size_t smem = 0;
-                if constexpr (ALGO == MR_TREE && reduce_top_shared(64, DT, VB, reduce_pairs(DT, OP, HOP))) {
-                    smem = reduce_top_shared_bytes(VB / Elem<DT>::kBytes);
-                    const cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-                    if (e != cudaSuccess) return e;
-                }
-                return launch_kernel(k, grid, smem, stream, 0, P);
-            }
+            case 32:
+                if constexpr (ALGO == MR_TREE) return launch_wide(std::integral_constant<int, 32>{});
+                return cudaErrorInvalidValue;
+            default:
+                return launch_wide(std::integral_constant<int, 64>{});
         }
     };
     switch (op) {

@@ -110,8 +110,9 @@ def _sizes(W):
 
 # W = 9 to 11 run the batched fold with 16 slots for every order, W = 12 the
 # plain 16-slot fold for the ring and the batched one for the tree, 13 and 16
-# the batched fold, 17 and up the batched fold with 64 slots
-CASES = [(W, N) for W in (1, 2, 3, 5, 8, 9, 11, 12, 13, 16, 17, 33, 64) for N in _sizes(W)]
+# the batched fold, 17 and up the batched fold with 64 slots, except the tree
+# up to 32 ranks (32 slots: 4 batch heads)
+CASES = [(W, N) for W in (1, 2, 3, 5, 8, 9, 11, 12, 13, 16, 17, 20, 32, 33, 64) for N in _sizes(W)]
 
 
 @pytest.mark.parametrize("W,N", CASES)
@@ -197,7 +198,7 @@ def test_in_place(mr, dtype):
 @pytest.mark.parametrize("dtype", DTYPES)
 @pytest.mark.parametrize("offset", [1, 2, 3])
 def test_unaligned_pointers(mr, dtype, offset):
-    for W in (3, 8, 16):
+    for W in (3, 8, 16, 20, 40):
         N = W * 1024 + 5
         for op in ("sum", "avg", "max"):
             host = _data(5000 + offset, W, N, dtype, op)
