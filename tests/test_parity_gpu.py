@@ -340,6 +340,24 @@ def test_int_counts_w16_full(mr):
                 assert_same(y.cpu().numpy(), want, f"int32 {op} {algo} rank {j}")
 
 
+@pytest.mark.parametrize("W,dtype,algo,N", [(19, "fp32", "ring", (1 << 19) + 5), (24, "bf16", "tree", (1 << 20) + 5),
+                                             (57, "int32", "ring", (1 << 19) + 5)])
+def test_grid_not_a_multiple_of_the_segments(mr, W, dtype, algo, N):
+    """Calls large enough for a full grid where the full grid (456 CTAs on 152
+    SMs) is a multiple of the segment count: the host takes a grid one or more
+    CTAs smaller; every element still matches the oracle."""
+    import torch
+    for op in ("sum", "max"):
+        host = _data(7000 + W, W, N, dtype, op)
+        xs = [to_device(h, dtype) for h in host]
+        ys = [torch.empty_like(x) for x in xs]
+        mr.mr_allreduce(xs, ys, op=op, algo=algo)
+        torch.cuda.synchronize()
+        want = oracle_allreduce(dtype, op, algo, host)
+        for j, y in enumerate(ys):
+            assert_same(to_host(y, dtype), want, f"allreduce {dtype} {op} {algo} W={W} rank {j}")
+
+
 def test_sweep_fp32_w8_full(mr):
     """W=8 fp32 Normal(0,1) sum at every sweep size: ring bit-exact; tree
     bit-exact to the oracle's tree order and within 2*W*2^-24*sum|y| of ring."""
