@@ -259,7 +259,8 @@ dim3 plan_tiles(mr::ReduceParams& P, int algo, int lanes, bool batched, bool wid
     const uint64_t vtiles = P.vec ? P.tiles_max * P.nseg : P.tile_start[P.nseg];
     const uint64_t tiles = std::max<uint64_t>(vtiles, (uint64_t)P.nseg);
     const int per_sm = mr::reduce_blocks_per_sm(mr::reduce_wcap(P.W, algo), u, batched, wide_heads);
-    uint64_t gx = std::min<uint64_t>((uint64_t)sm_count() * per_sm, tiles);
+    const uint64_t full = (uint64_t)sm_count() * per_sm;
+    uint64_t gx = std::min<uint64_t>(full, tiles);
     // Tile t goes to CTA t mod gx and segment t mod nseg, so with gx a
     // multiple of nseg every CTA stays on one segment for the whole call and
     // no CTA helps a segment that falls behind.  Above 8 segments (the batched
@@ -268,8 +269,9 @@ dim3 plan_tiles(mr::ReduceParams& P, int algo, int lanes, bool batched, bool wid
     // CTAs smaller, sharing no factor with nseg, deals every CTA's tiles
     // across all segments (5960, 6206, 6328).  Up to 8 segments (57 or more
     // CTAs per segment, the plain folds) the fixed assignment measured 3.6 %
-    // faster (W = 8 fp32 ring) and stays.
-    if (P.vec && P.nseg > 8 && gx % (uint64_t)P.nseg == 0) {
+    // faster (W = 8 fp32 ring) and stays.  A grid capped by the tile count
+    // (a small call: one tile per CTA, or a few) keeps one CTA per tile.
+    if (P.vec && P.nseg > 8 && gx == full && gx % (uint64_t)P.nseg == 0) {
         auto gcd = [](uint64_t a, uint64_t b) {
             while (b) {
                 const uint64_t t = a % b;
