@@ -42,6 +42,8 @@ struct ReduceParams {
     int group;      // hierarchical order: ranks per group
     int hop;        // 1: round a bf16 running total to bf16 after every combine
     uint64_t gmask; // hierarchical order: bit p set where order position p starts a group
+    uint32_t spread_smem;   // dynamic shared memory every CTA reserves at least, so that a
+                            // grid of fewer CTAs than resident slots spreads over the SMs
 };
 
 // All-reduce + residual + RMSNorm (rows x hidden elements).

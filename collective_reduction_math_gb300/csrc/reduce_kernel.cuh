@@ -783,6 +783,18 @@ reduce_kernel(const __grid_constant__ ReduceParams P) {
     }
 }
 
+// Launch with at least P.spread_smem bytes of dynamic shared memory per CTA
+// (see plan_tiles: it caps how many CTAs share an SM).
+template <class K>
+cudaError_t launch_spread(K k, dim3 grid, size_t smem, cudaStream_t stream, const ReduceParams& P) {
+    if (P.spread_smem > smem) smem = P.spread_smem;
+    if (smem > 48 * 1024) {
+        const cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        if (e != cudaSuccess) return e;
+    }
+    return launch_kernel(k, grid, smem, stream, 0, P);
+}
+
 // Instantiate and launch the kernel for one element type and one order.
 template <int DT, int ALGO, bool HOP>
 cudaError_t launch_reduce(const ReduceParams& P, int op, dim3 grid, cudaStream_t stream) {
@@ -796,23 +808,20 @@ cudaError_t launch_reduce(const ReduceParams& P, int op, dim3 grid, cudaStream_t
             constexpr int VB = reduce_vector_bytes(WC, ALGO, DT, OP, HOP);
             auto k = reduce_kernel<DT, OP, ALGO, WC, VB, reduce_unroll_for(WC, false), HOP, true>;
             size_t smem = 0;
-            if constexpr (reduce_top_shared(WC, ALGO)) {
+            if constexpr (reduce_top_shared(WC, ALGO))
                 smem = reduce_top_shared_bytes(WC, reduce_pairs(DT, OP, HOP) ? VB / 4 : VB / Elem<DT>::kBytes);
-                const cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-                if (e != cudaSuccess) return e;
-            }
-            return launch_kernel(k, grid, smem, stream, 0, P);
+            return launch_spread(k, grid, smem, stream, P);
         };
         switch (reduce_wcap(P.W, ALGO)) {
-            case 2: return launch_kernel(reduce_kernel<DT, OP, ALGO, 2, 16, reduce_unroll_for(2, false), HOP, false>, grid, 0, stream, 0, P);
-            case 4: return launch_kernel(reduce_kernel<DT, OP, ALGO, 4, 16, reduce_unroll_for(4, false), HOP, false>, grid, 0, stream, 0, P);
+            case 2: return launch_spread(reduce_kernel<DT, OP, ALGO, 2, 16, reduce_unroll_for(2, false), HOP, false>, grid, 0, stream, P);
+            case 4: return launch_spread(reduce_kernel<DT, OP, ALGO, 4, 16, reduce_unroll_for(4, false), HOP, false>, grid, 0, stream, P);
             case 8:
-                if (rs) return launch_kernel(reduce_kernel<DT, OP, ALGO, 8, 16, reduce_unroll_for(8, true), HOP, false>, grid, 0, stream, 0, P);
-                return launch_kernel(reduce_kernel<DT, OP, ALGO, 8, 16, reduce_unroll_for(8, false), HOP, false>, grid, 0, stream, 0, P);
+                if (rs) return launch_spread(reduce_kernel<DT, OP, ALGO, 8, 16, reduce_unroll_for(8, true), HOP, false>, grid, 0, stream, P);
+                return launch_spread(reduce_kernel<DT, OP, ALGO, 8, 16, reduce_unroll_for(8, false), HOP, false>, grid, 0, stream, P);
             case 16:
                 if (reduce_batched(P.W, ALGO, DT, HOP))
-                    return launch_kernel(reduce_kernel<DT, OP, ALGO, 16, 16, 1, HOP, true>, grid, 0, stream, 0, P);
-                return launch_kernel(reduce_kernel<DT, OP, ALGO, 16, 16, reduce_unroll_for(16, false), HOP, false>, grid, 0, stream, 0, P);
+                    return launch_spread(reduce_kernel<DT, OP, ALGO, 16, 16, 1, HOP, true>, grid, 0, stream, P);
+                return launch_spread(reduce_kernel<DT, OP, ALGO, 16, 16, reduce_unroll_for(16, false), HOP, false>, grid, 0, stream, P);
             case 32:
                 if constexpr (ALGO == MR_TREE) return launch_wide(std::integral_constant<int, 32>{});
                 return cudaErrorInvalidValue;
