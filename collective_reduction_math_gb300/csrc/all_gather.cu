@@ -106,8 +106,24 @@ all_gather_kernel(const __grid_constant__ GatherParams P) {
     }
 }
 
-cudaError_t launch_all_gather(const GatherParams& P, dim3 grid, cudaStream_t s) {
-    return launch_kernel(all_gather_kernel, grid, 0, s, 0, P);
+cudaError_t launch_all_gather(const GatherParams& P, dim3 grid, size_t smem, cudaStream_t s) {
+    if (smem > 48 * 1024) {
+        const cudaError_t e = cudaFuncSetAttribute(all_gather_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        if (e != cudaSuccess) return e;
+    }
+    return launch_kernel(all_gather_kernel, grid, smem, s, 0, P);
+}
+
+int all_gather_resident_per_sm() {
+    static int cached = 0;
+    if (cached > 0) return cached;
+    int n = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, all_gather_kernel, kThreads, 0) != cudaSuccess || n <= 0) {
+        cudaGetLastError();
+        return 1;
+    }
+    cached = n;
+    return n;
 }
 
 }  // namespace mr

@@ -457,9 +457,18 @@ mr_status_t mr_all_gather(const void* const* send, void* const* recv, int W, siz
     const uint64_t per_tile = P.vec ? (uint64_t)mr::kThreads * (mr::kGatherBytesPerThread / vb) : (uint64_t)mr::kThreads;
     const uint64_t units = P.vec ? (C * b) / vb : C;
     const uint64_t tiles = std::max<uint64_t>(1, (units + per_tile - 1) / per_tile) * (uint64_t)W;
-    const uint64_t gx = std::min<uint64_t>((uint64_t)sm_count() * mr::kGatherBlocksPerSm, tiles);
+    const uint64_t sms = (uint64_t)sm_count();
+    const uint64_t gx = std::min<uint64_t>(sms * mr::kGatherBlocksPerSm, tiles);
     const dim3 grid((unsigned)gx, 1, 1);
-    const cudaError_t err = mr::launch_all_gather(P, grid, (cudaStream_t)stream);
+    // A grid of more CTAs than SMs that still fits in one wave is spread as
+    // the reduce kernel's is (plan_tiles): at most ceil(gx / SMs) per SM.
+    size_t smem = 0;
+    const uint64_t resident = (uint64_t)mr::all_gather_resident_per_sm();
+    if (gx > sms && gx < sms * resident) {
+        const uint64_t cap = (gx + sms - 1) / sms;
+        if (cap < resident) smem = (227 * 1024) / (cap + 1) + 1024;
+    }
+    const cudaError_t err = mr::launch_all_gather(P, grid, smem, (cudaStream_t)stream);
     if (err != cudaSuccess) return fail(MR_ERR_CUDA, "all_gather launch failed: %s", cudaGetErrorString(err));
     g_launches.fetch_add(1, std::memory_order_relaxed);
     if (debug_level() > 0)

@@ -267,7 +267,10 @@ MR_DECLARE_REDUCE(int32, ring)
 MR_DECLARE_REDUCE(int32, tree)
 MR_DECLARE_REDUCE(int32, hier)
 #undef MR_DECLARE_REDUCE
-cudaError_t launch_all_gather(const GatherParams& P, dim3 grid, cudaStream_t s);
+// smem: dynamic shared memory each CTA reserves (none used; it caps residency).
+cudaError_t launch_all_gather(const GatherParams& P, dim3 grid, size_t smem, cudaStream_t s);
+// Resident all-gather CTAs per SM on the current device (its registers' limit).
+int all_gather_resident_per_sm();
 mr_status_t report_error(mr_status_t st, const char* fmt, ...);
 cudaError_t launch_sign_l1(const SignParams& P, cudaStream_t s);
 // Supplies a workspace (pointer and size) for the sign path.
