@@ -50,7 +50,7 @@ def batch_top(yb, Wb):
 
 
 def batched_fold(W, slots, swap_children=False):
-    """The kernel's schedule with `slots` register slots (16 or 64).
+    """The kernel's schedule with `slots` register slots (16, 32 or 64).
     swap_children plants a mistake: a head adds its upper child first."""
     y = [f"y{i}" for i in range(W)] + [None] * (slots + 8 - W)
     NB, M = slots // 8, (W + 7) // 8
@@ -87,15 +87,26 @@ def batched_fold(W, slots, swap_children=False):
     return a
 
 
+def kernel_slots(W):
+    """The slots of the kernel the host runs for the tree: 16 up to 16 ranks,
+    32 (4 batch heads) up to 32, else 64 (8 heads)."""
+    return 16 if W <= 16 else 32 if W <= 32 else 64
+
+
 @pytest.mark.parametrize("W", range(9, 65))
 def test_batched_tree_is_the_oracle_tree(oracle_mod, W):
-    slots = 16 if W <= 16 else 64
-    assert batched_fold(W, slots) == oracle_fold(W, oracle_mod)
+    assert batched_fold(W, kernel_slots(W)) == oracle_fold(W, oracle_mod)
+
+
+@pytest.mark.parametrize("W", range(17, 33))
+def test_the_64_slot_tree_also_folds_17_to_32_ranks(oracle_mod, W):
+    """The 64-slot schedule over at most 4 batches is the 32-slot one."""
+    assert batched_fold(W, 64) == batched_fold(W, 32) == oracle_fold(W, oracle_mod)
 
 
 @pytest.mark.parametrize("W", [12, 24, 64])
 def test_a_planted_mistake_is_caught(oracle_mod, W):
     """A head that adds its upper child before its lower one is caught."""
-    slots = 16 if W <= 16 else 64
+    slots = kernel_slots(W)
     assert batched_fold(W, slots) == oracle_fold(W, oracle_mod)
     assert batched_fold(W, slots, swap_children=True) != oracle_fold(W, oracle_mod)
