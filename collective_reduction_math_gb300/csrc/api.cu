@@ -357,9 +357,9 @@ mr_status_t run_reduce(const char* what, int mode, const void* const* send, void
         fprintf(stderr, "[mr] %s auto -> %s (model %.2f us)\n", what, algo_name(algo), predicted);
     if (debug_level() > 0)
         fprintf(stderr, "[mr] %s dtype=%s op=%s algo=%s group=%d per_hop=%d W=%d N=%zu segments=%d tiles=%llu "
-                "vector=%d grid=%u threads=%d\n",
+                "vector=%d grid=%u threads=%d spread_smem=%u sms=%d\n",
                 what, dtype_name(dtype), op_name(op), algo_name(algo), P.group, P.hop, W, N, P.nseg,
-                (unsigned long long)P.tile_start[P.nseg], P.vec, grid.x, mr::kThreads);
+                (unsigned long long)P.tile_start[P.nseg], P.vec, grid.x, mr::kThreads, P.spread_smem, sm_count());
     return MR_OK;
 }
 
