@@ -240,6 +240,23 @@ int plan_segments_hier(int W, uint64_t N, int group, bool cut_at_chunks, mr::Seg
     return n;
 }
 
+// Dynamic shared memory each CTA of a one-wave grid reserves so that the
+// grid spreads over the SMs: with more than 1.25 CTAs per SM but fewer than
+// the resident slots, the block scheduler measured to put up to `resident`
+// CTAs on some SMs while others stayed idle; reserving 227 KB / (cap + 1)
+// per CTA leaves room for at most cap = ceil(grid / SMs).  Measured (back to
+// back, warm L2): the W = 8 fp32 all-reduce at 228-300 tiles 13-17 % faster,
+// W = 32 at 200 tiles 11 %, the all-gather at 256 CTAs 17-24 %, the fused
+// RMSNorm at 256-300 rows 13-16 %; from 1.05 to 1.25 CTAs per SM it cost
+// up to 3 % and is not taken.  0: no reservation.
+size_t spread_smem(uint64_t grid, uint64_t resident) {
+    const uint64_t sms = (uint64_t)sm_count();
+    if (4 * grid <= 5 * sms || grid >= sms * resident) return 0;
+    const uint64_t cap = (grid + sms - 1) / sms;
+    if (cap >= resident) return 0;
+    return (size_t)((227 * 1024) / (cap + 1) + 1024);
+}
+
 dim3 plan_tiles(mr::ReduceParams& P, int algo, int lanes, bool batched, bool wide_heads) {
     const bool rs = P.mode == mr::MODE_REDUCE_SCATTER;
     const int u = mr::reduce_unroll(P.W, algo, rs);
@@ -282,19 +299,10 @@ dim3 plan_tiles(mr::ReduceParams& P, int algo, int lanes, bool batched, bool wid
         };
         while (gx > 1 && gcd(gx, (uint64_t)P.nseg) != 1) --gx;
     }
-    // A grid with more CTAs than SMs but fewer than the resident slots: the
-    // block scheduler measured to put up to per_sm of them on some SMs while
-    // others stayed idle.  Each CTA then reserves enough shared memory that
-    // at most ceil(gx / SMs) share an SM.  Measured at 1 MiB per rank (256 CTAs
-    // of a 456-slot grid, inputs warm in L2), back to back: W = 8 fp32 ring
-    // 3.43 -> 3.02 us, W = 16 5.67 -> 4.83, W = 32 10.08 -> 8.52, W = 64
-    // 26.1 -> 23.3; the other sizes unchanged.
-    P.spread_smem = 0;
-    const uint64_t sms = (uint64_t)sm_count();
-    if (gx > sms && gx < full) {
-        const uint64_t cap = (gx + sms - 1) / sms;
-        if (cap < (uint64_t)per_sm) P.spread_smem = (uint32_t)((227 * 1024) / (cap + 1) + 1024);
-    }
+    // A one-wave grid with more CTAs than SMs is spread over them (at 1 MiB
+    // per rank, 256 CTAs: W = 8 fp32 ring 3.43 -> 3.02 us, W = 16 5.67 ->
+    // 4.83, W = 32 10.08 -> 8.52, W = 64 26.1 -> 23.3).
+    P.spread_smem = (uint32_t)spread_smem(gx, (uint64_t)per_sm);
     return dim3((unsigned)std::max<uint64_t>(gx, 1), 1, 1);
 }
 
@@ -460,14 +468,8 @@ mr_status_t mr_all_gather(const void* const* send, void* const* recv, int W, siz
     const uint64_t sms = (uint64_t)sm_count();
     const uint64_t gx = std::min<uint64_t>(sms * mr::kGatherBlocksPerSm, tiles);
     const dim3 grid((unsigned)gx, 1, 1);
-    // A grid of more CTAs than SMs that still fits in one wave is spread as
-    // the reduce kernel's is (plan_tiles): at most ceil(gx / SMs) per SM.
-    size_t smem = 0;
-    const uint64_t resident = (uint64_t)mr::all_gather_resident_per_sm();
-    if (gx > sms && gx < sms * resident) {
-        const uint64_t cap = (gx + sms - 1) / sms;
-        if (cap < resident) smem = (227 * 1024) / (cap + 1) + 1024;
-    }
+    // A one-wave grid of more CTAs than SMs is spread over them.
+    const size_t smem = spread_smem(gx, (uint64_t)mr::all_gather_resident_per_sm());
     const cudaError_t err = mr::launch_all_gather(P, grid, smem, (cudaStream_t)stream);
     if (err != cudaSuccess) return fail(MR_ERR_CUDA, "all_gather launch failed: %s", cudaGetErrorString(err));
     g_launches.fetch_add(1, std::memory_order_relaxed);
@@ -644,6 +646,9 @@ mr_status_t mr_allreduce_rmsnorm(const void* const* send, void* const* recv, int
     }
     const size_t clusters = std::min<size_t>(rows, std::max<size_t>(1, sms * per_sm / csize));
     const dim3 grid((unsigned)(clusters * csize), 1, 1);
+    // A one-wave grid of more CTAs than SMs is spread over them (W = 8 bf16,
+    // hidden 8192, 256 and 300 rows: 17.3 -> 15.1 us, 19.9 -> 16.7 us).
+    smem = std::max<size_t>(smem, spread_smem(grid.x, per_sm));
     const cudaError_t err = mr::launch_allreduce_rmsnorm(P, dtype, algo, grid, smem, (cudaStream_t)stream);
     if (err != cudaSuccess) return fail(MR_ERR_CUDA, "allreduce_rmsnorm launch failed: %s", cudaGetErrorString(err));
     g_launches.fetch_add(1, std::memory_order_relaxed);

@@ -1,8 +1,9 @@
 """The reduce kernel's grid, as the library reports it with MR_DEBUG=1.
 
 The host sizes the grid (plan_tiles): one CTA per tile up to the resident
-slots (3 or 2 per SM); a mid-size grid (more CTAs than SMs, fewer than the
-slots) reserves shared memory so that at most ceil(G / SMs) CTAs share an SM;
+slots (3 or 2 per SM); a mid-size grid (more than 1.25 CTAs per SM, fewer
+than the slots) reserves shared memory so that at most ceil(G / SMs) CTAs
+share an SM;
 a full grid that is a multiple of more than 8 segments is cut to the largest
 grid that shares no factor with the segment count.  Each call here runs in a
 child process with MR_DEBUG=1 and its reported grid is checked against those
@@ -62,12 +63,16 @@ def test_small_calls_keep_one_cta_per_tile():
 
 
 def test_mid_size_grids_spread_over_the_sms():
-    """More tiles than SMs but fewer than the slots: one CTA per tile, with
-    enough shared memory reserved that at most ceil(G / SMs) share an SM."""
-    calls = [(8, 1 << 18, "ring"), (32, 1 << 18, "ring"), (16, 1 << 18, "tree")]
+    """More than 1.25 tiles per SM but fewer than the slots: one CTA per tile,
+    with enough shared memory reserved that at most ceil(G / SMs) share an
+    SM; at 1.05 tiles per SM (160 tiles) nothing is reserved."""
+    calls = [(8, 1 << 18, "ring"), (32, 1 << 18, "ring"), (16, 1 << 18, "tree"), (8, 160 * 1024, "ring")]
     for W, N, nseg, tiles, vec, grid, spread, sms in reported(calls):
         assert sms < tiles < 3 * sms, (W, tiles, sms)
         assert grid == tiles
+        if 4 * grid <= 5 * sms:
+            assert spread == 0, (W, grid, spread)
+            continue
         cap = -(-grid // sms)
         assert spread > 0
         assert (cap + 1) * (spread + 1024) > 228 * 1024 >= cap * (spread + 1024), (W, cap, spread)
