@@ -349,7 +349,7 @@ mr_status_t run_reduce(const char* what, int mode, const void* const* send, void
     P.nseg = algo == MR_HIER ? plan_segments_hier(W, N, group, mode == mr::MODE_REDUCE_SCATTER, P.seg)
                              : plan_segments(W, N, algo, P.seg);
     const int eb = (int)elem_bytes(dtype);
-    const int vb = mr::reduce_vector_bytes(W, algo, dtype, op, hop != 0);
+    const int vb = mr::kReduceVectorBytes;
     bool vec = true;
     for (int r = 0; r < W; ++r)
         vec = vec && ((uintptr_t)send[r] % vb == 0) && ((uintptr_t)recv[r] % vb == 0);

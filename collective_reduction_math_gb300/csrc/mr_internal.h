@@ -145,14 +145,12 @@ constexpr bool reduce_pairs(int dtype, int op, bool hop) {
     return dtype == MR_BF16 && hop && (op == MR_SUM || op == MR_AVG);
 }
 // Every variant of the reduce kernel moves 16-byte vectors; the host's
-// alignment check and the kernel's template both take the width from here.
-constexpr int reduce_vector_bytes(int W, int algo, int dtype, int op, bool hop) {
-    (void)W; (void)algo; (void)dtype; (void)op; (void)hop;
-    return 16;
-}
-// The batched tree over 64 slots keeps its 8 batches' in-batch top subtotals
-// (one per unit: a lane, or a packed pair of bf16 lanes) in shared memory,
-// per thread, instead of registers: each is written once and read once.
+// alignment check and the kernel's templates both take the width from here.
+constexpr int kReduceVectorBytes = 16;
+// The batched trees over 32 and 64 slots keep their batches' in-batch top
+// subtotals (one per unit: a lane, or a packed pair of bf16 lanes) in shared
+// memory, per thread, instead of registers: each is written once and read
+// once.
 constexpr bool reduce_top_shared(int wcap, int algo) { return wcap >= 32 && algo == MR_TREE; }
 constexpr size_t reduce_top_shared_bytes(int wcap, int units) {
     return (size_t)(wcap / 8) * units * kThreads * sizeof(uint32_t);

@@ -805,7 +805,7 @@ cudaError_t launch_reduce(const ReduceParams& P, int op, dim3 grid, cudaStream_t
         // dynamic shared memory.
         auto launch_wide = [&](auto wc) -> cudaError_t {
             constexpr int WC = decltype(wc)::value;
-            constexpr int VB = reduce_vector_bytes(WC, ALGO, DT, OP, HOP);
+            constexpr int VB = kReduceVectorBytes;
             auto k = reduce_kernel<DT, OP, ALGO, WC, VB, reduce_unroll_for(WC, false), HOP, true>;
             size_t smem = 0;
             if constexpr (reduce_top_shared(WC, ALGO))
