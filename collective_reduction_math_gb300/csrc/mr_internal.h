@@ -140,9 +140,11 @@ struct GatherParams {
 constexpr int reduce_wcap(int W, int algo) {
     return W <= 2 ? 2 : W <= 4 ? 4 : W <= 8 ? 8 : W <= 16 ? 16 : (algo == MR_TREE && W <= 32) ? 32 : 64;
 }
-// Per-hop bf16 sum and avg fold packed pairs (two lanes per 32-bit word).
+// Per-hop bf16 sum and avg, and bf16 min and max (on 16-bit order keys; not
+// in the plain 16-slot fold), fold packed pairs (two lanes per 32-bit word).
+// The host asks this of the batched trees over 32 and 64 slots only.
 constexpr bool reduce_pairs(int dtype, int op, bool hop) {
-    return dtype == MR_BF16 && hop && (op == MR_SUM || op == MR_AVG);
+    return dtype == MR_BF16 && ((hop && (op == MR_SUM || op == MR_AVG)) || op == MR_MIN || op == MR_MAX);
 }
 // Every variant of the reduce kernel moves 16-byte vectors; the host's
 // alignment check and the kernel's templates both take the width from here.
@@ -184,7 +186,9 @@ constexpr int reduce_blocks_per_sm(int wcap, int u, bool batch, bool wide_heads)
 //   rings (and the hierarchical order) at 9 to 11 ranks: bf16 max W = 9
 //     5.58 -> 5.92, per-hop bf16 avg W = 10 5.26 -> 6.21;
 //   at 12 ranks the plain ring stays 1-3.5 % ahead (bf16 max 6.23 against
-//     6.01), except per-hop (5.75 -> 6.03);
+//     6.01), except per-hop (5.75 -> 6.03); the hierarchical order does not
+//     (groups of 3, 4 or 6: fp32 sum 5.48-5.50 -> 6.27-6.28, bf16 max
+//     4.83-4.87 -> 6.16-6.19, int32 sum 5.28-5.32 -> 6.24-6.26);
 //   from 13 ranks every order batched (at W = 16 with 3 CTAs per SM: int32
 //     sum ring 5.88 -> 6.28 at 16 MiB per rank, per-hop bf16 ring 6.10 ->
 //     6.37).
@@ -193,7 +197,7 @@ constexpr bool reduce_batched(int W, int algo, int dtype, bool hop) {
     (void)dtype;
     if (W >= kBatchFromRanks) return true;
     if (W <= 8) return false;
-    if (algo == MR_TREE) return true;
+    if (algo == MR_TREE || algo == MR_HIER) return true;
     return W < 12 || hop;
 }
 

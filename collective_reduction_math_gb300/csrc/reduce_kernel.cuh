@@ -130,6 +130,35 @@ struct Bf16PairSum {
     static __device__ __forceinline__ acc_t hop(acc_t a) { return a; }
 };
 
+// bf16 min and max on packed pairs.  The 16-bit order key of a bf16 value
+// (x with its 15 magnitude bits flipped when the sign bit is set) orders
+// exactly as the 32-bit key of its fp32 widening, whose low half is then 0 or
+// 0xFFFF with the sign; so the two lanes of a word fold as signed 16-bit
+// keys, one vmin2 / vmax2 per pair, with the lane-wise fold's result.  The
+// map is its own inverse.
+template <int OP> struct Bf16PairKey {
+    using acc_t = uint32_t;
+    static __device__ __forceinline__ uint32_t key(uint32_t w) {
+        return w ^ (((w >> 15) & 0x00010001u) * 0x7FFFu);
+    }
+    static __device__ __forceinline__ acc_t combine(acc_t a, acc_t b) {
+        if constexpr (OP == MR_MIN) return __vmins2(a, b);
+        else return __vmaxs2(a, b);
+    }
+    static __device__ __forceinline__ acc_t hop(acc_t a) { return a; }
+    // The two bf16 results: the keys mapped back, each lane then rounded to
+    // bf16 from its fp32 widening in one packed conversion, as the lane-wise
+    // fold's postOp does (the identity but for NaN, which the conversion
+    // makes canonical).
+    static __device__ __forceinline__ uint32_t post(acc_t k) {
+        const uint32_t w = key(k);
+        const __nv_bfloat162 p = __floats2bfloat162_rn(__uint_as_float(w << 16), __uint_as_float(w & 0xFFFF0000u));
+        uint32_t o;
+        memcpy(&o, &p, 4);
+        return o;
+    }
+};
+
 // ---------------------------------------------------------------------------
 // The folds.  y[p] holds the contribution at order position p; only the
 // first W positions are valid.  All register indices are compile-time.
@@ -504,8 +533,12 @@ reduce_kernel(const __grid_constant__ ReduceParams P) {
     const float s = P.scale;
     const bool rs = (P.mode == MODE_REDUCE_SCATTER);
     constexpr bool hop = DT == MR_BF16 && HOP;
-    // per-hop bf16 sum / avg: fold two lanes per packed word (Bf16PairSum)
-    constexpr bool kPairs = DT == MR_BF16 && HOP && (OP == MR_SUM || OP == MR_AVG);   // reduce_pairs()
+    // Two bf16 lanes per packed word: per-hop sum and avg (Bf16PairSum), and
+    // min and max on 16-bit order keys (Bf16PairKey) except in the plain
+    // 16-slot fold, where the keyed pairs spilled and ran 4-14 % slower.
+    constexpr bool kPairKeys = DT == MR_BF16 && (OP == MR_MIN || OP == MR_MAX) && (BATCH || WCAP <= 8);
+    constexpr bool kPairs = kPairKeys || (DT == MR_BF16 && HOP && (OP == MR_SUM || OP == MR_AVG));   // reduce_pairs()
+    using PairA = typename std::conditional<kPairKeys, Bf16PairKey<OP>, Bf16PairSum>::type;
     const uint64_t gmask = P.gmask;
     // a contribution as read: widened, pre-scaled, and for per-hop bf16 rounded
     auto contrib = [&](raw_t x) -> acc_t {
@@ -513,11 +546,13 @@ reduce_kernel(const __grid_constant__ ReduceParams P) {
         return (OP == MR_AVG && hop) ? A::hop(y) : y;
     };
 
-    // Per-hop pairs: one 32-bit word holds two bf16 contributions as read
-    // (avg: pre-scaled in fp32, both lanes rounded to bf16 in one packed
-    // conversion, lo lane in x).
+    // Pairs: one 32-bit word holds two bf16 contributions as read (avg:
+    // pre-scaled in fp32, both lanes rounded to bf16 in one packed conversion,
+    // lo lane in x; min and max: their 16-bit order keys).
     auto pair = [&](uint32_t w) -> uint32_t {
-        if constexpr (OP == MR_AVG) {
+        if constexpr (kPairKeys) {
+            return Bf16PairKey<OP>::key(w);
+        } else if constexpr (OP == MR_AVG) {
             const float lo = __fmul_rn(__uint_as_float(w << 16), s);
             const float hi = __fmul_rn(__uint_as_float(w & 0xFFFF0000u), s);
             const __nv_bfloat162 p = __floats2bfloat162_rn(lo, hi);
@@ -529,7 +564,7 @@ reduce_kernel(const __grid_constant__ ReduceParams P) {
         }
     };
     // The batched folds run on "units": a lane's fp32 (or int32) value, or
-    // with per-hop pairs a packed word of two bf16 lanes.
+    // with pairs a packed word of two bf16 lanes.
     using unit_t = typename std::conditional<kPairs, uint32_t, acc_t>::type;
     constexpr int UNITS = kPairs ? VB / 4 : LANES;
     auto unit = [&](const Vec<VB>& v, int u) -> unit_t {
@@ -537,17 +572,22 @@ reduce_kernel(const __grid_constant__ ReduceParams P) {
         else return contrib(get_lane<raw_t, VB>(v, u));
     };
     auto ucomb = [&](unit_t a, unit_t b) -> unit_t {
-        if constexpr (kPairs) return Bf16PairSum::combine(a, b);
+        if constexpr (kPairs) return PairA::combine(a, b);
         else return comb<A>(a, b, hop);
     };
     auto utop = [&](unit_t (&y)[8], int Wb) -> unit_t {
-        if constexpr (kPairs) return tree_batch_top<Bf16PairSum>(y, Wb, false);
+        if constexpr (kPairs) return tree_batch_top<PairA>(y, Wb, false);
         else return tree_batch_top<A>(y, Wb, hop);
+    };
+    // A pair's result: the packed sum itself, or the keys' bf16 values.
+    auto pair_post = [&](uint32_t r) -> uint32_t {
+        if constexpr (kPairKeys) return Bf16PairKey<OP>::post(r);
+        else return r;
     };
     auto upost = [&](const unit_t (&r)[UNITS], Vec<VB>& res) {
         if constexpr (kPairs) {
 #pragma unroll
-            for (int u = 0; u < UNITS; ++u) res.w[u] = r[u];
+            for (int u = 0; u < UNITS; ++u) res.w[u] = pair_post(r[u]);
         } else {
 #pragma unroll
             for (int l = 0; l < LANES; ++l) set_lane<raw_t, VB>(res, l, A::post(r[l], W));
@@ -739,7 +779,7 @@ reduce_kernel(const __grid_constant__ ReduceParams P) {
 #pragma unroll
                             for (int i = 0; i < WCAP; ++i)
                                 if (i < W) y[i] = pair(raw[u][i].w[k]);
-                            res.w[k] = fold<Bf16PairSum, ALGO, WCAP>(y, W, false, gmask);
+                            res.w[k] = pair_post(fold<PairA, ALGO, WCAP>(y, W, false, gmask));
                         }
                     } else {
                         acc_t r[LANES];
