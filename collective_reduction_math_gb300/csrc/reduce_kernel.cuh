@@ -611,9 +611,8 @@ reduce_kernel(const __grid_constant__ ReduceParams P) {
     // barriers while the CTA's other warps run on.  The other batched folds
     // (3 CTAs per SM) share one table per CTA: there the CTA-wide barrier
     // measured faster (warps that stay on one tile together, 3-6 % at 10-28
-    // ranks), at 2 CTAs per SM slower (the 64-slot trees 4-12 %), except for
-    // bf16 min and max (2-5 % faster with the CTA's table at 57 and 64 ranks).
-    constexpr bool kWarpTable = kTable && WCAP == 64 && ALGO == MR_TREE && !(DT == MR_BF16 && A::kKeyed);
+    // ranks), at 2 CTAs per SM slower (the 64-slot trees 3-12 %).
+    constexpr bool kWarpTable = kTable && WCAP == 64 && ALGO == MR_TREE;
     constexpr int kTables = kWarpTable ? kThreads / 32 : 1;
     __shared__ const char* table[kTables][kTable ? WCAP : 1];
     const char* src[kTable ? 1 : WCAP];
