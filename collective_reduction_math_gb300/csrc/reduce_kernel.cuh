@@ -90,6 +90,26 @@ template <int DT, int OP> struct Arith {
         }
     }
 
+    // The op's identity element e, exact in both orders (combine(a, e) and
+    // combine(e, a) are a, bit for bit, for every value a the folds carry,
+    // NaN and signed zeros included): -0.0 for float sums (x + -0.0 = x under
+    // round-to-nearest, and -0.0 + -0.0 = -0.0), 1 for products, the extreme
+    // keys for min and max, 0 for integer sums.  The batched tree pads the
+    // positions past W with it.
+    static __device__ __forceinline__ acc_t identity() {
+        if constexpr (DT == MR_INT32) {
+            if constexpr (OP == MR_SUM || OP == MR_AVG) return 0u;
+            if constexpr (OP == MR_PROD) return 1u;
+            if constexpr (OP == MR_MIN) return 0x7FFFFFFFu;
+            if constexpr (OP == MR_MAX) return 0x80000000u;
+        } else {
+            if constexpr (OP == MR_SUM || OP == MR_AVG) return -0.0f;
+            if constexpr (OP == MR_PROD) return 1.0f;
+            if constexpr (OP == MR_MIN) return __int_as_float(0x7FFFFFFF);
+            if constexpr (OP == MR_MAX) return __int_as_float((int)0x80000000u);
+        }
+    }
+
     // Per-hop rounding: a bf16 running total rounded to bf16 (as it would
     // cross a wire); the identity for fp32 and int32, and for min and max,
     // whose running value is always one of the bf16 contributions.
@@ -127,6 +147,7 @@ struct Bf16PairSum {
         memcpy(&o, &r, 4);
         return o;
     }
+    static __device__ __forceinline__ acc_t identity() { return 0x80008000u; }   // -0.0 in both lanes
     static __device__ __forceinline__ acc_t hop(acc_t a) { return a; }
 };
 
@@ -145,6 +166,8 @@ template <int OP> struct Bf16PairKey {
         if constexpr (OP == MR_MIN) return __vmins2(a, b);
         else return __vmaxs2(a, b);
     }
+    // The extreme signed 16-bit key in both lanes.
+    static __device__ __forceinline__ acc_t identity() { return OP == MR_MIN ? 0x7FFF7FFFu : 0x80008000u; }
     static __device__ __forceinline__ acc_t hop(acc_t a) { return a; }
     // The two bf16 results: the keys mapped back, each lane then rounded to
     // bf16 from its fp32 widening in one packed conversion, as the lane-wise
@@ -363,6 +386,62 @@ __device__ __forceinline__ void batched_tree(int W, Load load, Unit unit, Comb c
     }
 }
 
+// The same tree over padded positions (the int32 trees over 16 slots take
+// it): the positions past W are padded with the op's exact identity e and the
+// fold runs the whole tree over NB batches of 8, with no condition on W but
+// which positions to load: each head's upper child is head m + B/2 (B > 1)
+// or its own batch's node 4, each in-batch node's upper child p + b/2.  A
+// subtree of the padded tree whose positions all lie past W is e; one whose
+// upper child's subtree is e takes, in place of the real tree's next smaller
+// upper child, the padded child's lower subtree, which is that child.  So
+// every node folds the real tree's operands in the real tree's order, with
+// extra combines with e that change no bit: these are fold_tree's results.
+template <int NB, int UNITS, class T, class R, class Load, class Unit, class Comb, class Ident, class TopAt>
+__device__ __forceinline__ void batched_tree_padded(int W, Load load, Unit unit, Comb comb, Ident ident, TopAt top_at,
+                                                    T (&root)[UNITS]) {
+    const int M = (W + 7) >> 3;
+    T head[NB][UNITS];
+#pragma unroll
+    for (int m = 0; m < NB; ++m) {
+        if (m < M) {
+            const int Wb = min(8, W - 8 * m);
+            R raw[8];
+            load(m, Wb, raw);
+#pragma unroll
+            for (int u = 0; u < UNITS; ++u) {
+                T y[8];
+#pragma unroll
+                for (int q = 0; q < 8; ++q) y[q] = q < Wb ? unit(raw[q], u) : ident();
+                // levels 2 and 4 inside the batch
+                y[2] = comb(comb(y[2], y[1]), y[3]);
+                y[6] = comb(comb(y[6], y[5]), y[7]);
+                y[4] = comb(comb(y[4], y[2]), y[6]);
+                head[m][u] = y[0];
+                top_at(m, u) = y[4];
+            }
+        } else {
+#pragma unroll
+            for (int u = 0; u < UNITS; ++u) {
+                head[m][u] = ident();
+                top_at(m, u) = ident();
+            }
+        }
+    }
+#pragma unroll
+    for (int B = 1; B < NB; B <<= 1) {
+#pragma unroll
+        for (int m = B; m < NB; m += 2 * B) {
+#pragma unroll
+            for (int u = 0; u < UNITS; ++u) {
+                T a = comb(head[m][u], B == 1 ? top_at(m - 1, u) : head[m - B / 2][u]);
+                head[m][u] = comb(a, B == 1 ? top_at(m, u) : head[m + B / 2][u]);
+            }
+        }
+    }
+#pragma unroll
+    for (int u = 0; u < UNITS; ++u) root[u] = NB > 1 ? comb(head[0][u], head[NB / 2][u]) : comb(head[0][u], top_at(0, u));
+}
+
 // Hierarchical: positions come group by group (gmask marks the first position
 // of each group); each group's positions are folded left to right, then the
 // group totals left to right.
@@ -579,6 +658,10 @@ reduce_kernel(const __grid_constant__ ReduceParams P) {
         if constexpr (kPairs) return tree_batch_top<PairA>(y, Wb, false);
         else return tree_batch_top<A>(y, Wb, hop);
     };
+    auto uident = []() -> unit_t {
+        if constexpr (kPairs) return PairA::identity();
+        else return A::identity();
+    };
     // A pair's result: the packed sum itself, or the keys' bf16 values.
     auto pair_post = [&](uint32_t r) -> uint32_t {
         if constexpr (kPairKeys) return Bf16PairKey<OP>::post(r);
@@ -600,6 +683,12 @@ reduce_kernel(const __grid_constant__ ReduceParams P) {
     // vectors are live at a time).
     constexpr bool kTable = BATCH;
     constexpr bool kTreeBatched = BATCH && ALGO == MR_TREE;
+    // The int32 trees over 16 slots fold the identity-padded tree (no
+    // condition on W inside a batch): at 9-11 ranks the conditional fold's
+    // branches (3x the ring's, ncu) held them at 5.67-5.84 TB/s; padded they
+    // run at 5.89-6.35 (sum 6.22-6.35).  The float trees measured slower
+    // padded (fp32 at 9-13 ranks 4-10 %) and keep the conditional fold.
+    constexpr bool kPaddedTree = kTreeBatched && DT == MR_INT32 && WCAP == 16;
     // The 32- and 64-slot trees keep their batches' top subtotals in dynamic
     // shared memory (see reduce_top_shared).
     constexpr bool kTopShared = kTreeBatched && WCAP >= 32;   // reduce_top_shared()
@@ -738,7 +827,10 @@ reduce_kernel(const __grid_constant__ ReduceParams P) {
                             if constexpr (kTopShared) return top_smem[((uint64_t)m * UNITS + u) * kThreads + threadIdx.x];
                             else return top_reg[m][u];
                         };
-                        batched_tree<NB, UNITS, unit_t, Vec<VB>>(W, load, unit, ucomb, utop, top_at, res_u);
+                        if constexpr (kPaddedTree)
+                            batched_tree_padded<NB, UNITS, unit_t, Vec<VB>>(W, load, unit, ucomb, uident, top_at, res_u);
+                        else
+                            batched_tree<NB, UNITS, unit_t, Vec<VB>>(W, load, unit, ucomb, utop, top_at, res_u);
                     } else {
                         batched_left_fold<ALGO == MR_HIER, UNITS, unit_t, Vec<VB>>(W, gmask, load, unit, ucomb, res_u);
                     }

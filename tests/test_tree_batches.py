@@ -5,8 +5,11 @@ From 13 ranks up the CUDA kernel does not hold all W contributions of an
 element at once.  It loads the positions in batches [8m, 8m+8), folds each
 batch up to the node that the batch head's upper-child search finds inside it,
 and then folds the batch heads 8m as the same bit-trick tree one level up.
-This test restates that schedule on symbols and checks, for every W from 9 to
-64, that it performs the oracle's combines in the oracle's order: each node's
+The int32 trees over 16 slots run a second schedule: the positions past W
+padded with the op's exact identity and the whole tree folded with no
+condition on W.  This test restates both schedules on symbols and checks,
+for every W from 9 to 64, that they perform the oracle's combines in the
+oracle's order (the padded one once its identities drop): each node's
 own value first, then its children's subtotals in the order the oracle lists
 them (double binary tree, "The double binary tree", post on NCCL all-reduce).
 Positions, not ranks, are folded, so one check covers both trees.
@@ -87,6 +90,42 @@ def batched_fold(W, slots, swap_children=False):
     return a
 
 
+def cmb(a, b):
+    """One combine, written out; the identity e drops (a + e = e + a = a)."""
+    if a == "e":
+        return b
+    if b == "e":
+        return a
+    return f"({a}+{b})"
+
+
+def padded_fold(W, slots, swap_children=False):
+    """The kernel's schedule: positions past W padded with the identity e and
+    the whole bit-trick tree over slots // 8 batches of 8 folded with no
+    condition on W (in-batch nodes 2, 6, 4; head m's lower child the previous
+    batch's node 4 or head m - B/2, its upper child its own batch's node 4 or
+    head m + B/2; the root's child head NB/2).  swap_children plants a
+    mistake: a head adds its upper child first."""
+    NB = slots // 8
+    y = [f"y{i}" if i < W else "e" for i in range(slots)]
+    head, top = [None] * NB, [None] * NB
+    for m in range(NB):
+        b = y[8 * m:8 * m + 8]
+        n2 = cmb(cmb(b[2], b[1]), b[3])
+        n6 = cmb(cmb(b[6], b[5]), b[7])
+        top[m] = cmb(cmb(b[4], n2), n6)
+        head[m] = b[0]
+    B = 1
+    while B < NB:
+        for m in range(B, NB, 2 * B):
+            lower = top[m - 1] if B == 1 else head[m - B // 2]
+            upper = top[m] if B == 1 else head[m + B // 2]
+            first, second = (upper, lower) if swap_children else (lower, upper)
+            head[m] = cmb(cmb(head[m], first), second)
+        B *= 2
+    return cmb(head[0], head[NB // 2])
+
+
 def kernel_slots(W):
     """The slots of the kernel the host runs for the tree: 16 up to 16 ranks,
     32 (4 batch heads) up to 32, else 64 (8 heads)."""
@@ -110,3 +149,17 @@ def test_a_planted_mistake_is_caught(oracle_mod, W):
     slots = kernel_slots(W)
     assert batched_fold(W, slots) == oracle_fold(W, oracle_mod)
     assert batched_fold(W, slots, swap_children=True) != oracle_fold(W, oracle_mod)
+
+
+@pytest.mark.parametrize("W", range(9, 65))
+def test_padded_tree_is_the_oracle_tree(oracle_mod, W):
+    """The identity-padded schedule the kernel runs gives the oracle's tree
+    fold once the identities drop, at the host's slot count and at 64."""
+    want = oracle_fold(W, oracle_mod)
+    assert padded_fold(W, kernel_slots(W)) == want
+    assert padded_fold(W, 64) == want
+
+
+@pytest.mark.parametrize("W", [10, 12, 24, 40, 64])
+def test_a_planted_mistake_in_the_padded_tree_is_caught(oracle_mod, W):
+    assert padded_fold(W, kernel_slots(W), swap_children=True) != oracle_fold(W, oracle_mod)
