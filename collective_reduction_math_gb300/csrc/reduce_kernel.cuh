@@ -598,7 +598,7 @@ __device__ __forceinline__ int order_rank(int W, const Segment& sg, int i, int g
     else return hier_rank(W, group, sg.hc, sg.hd, i);
 }
 
-template <int DT, int OP, int ALGO, int WCAP, int VB, int U, bool HOP, bool BATCH>
+template <int DT, int OP, int ALGO, int WCAP, int VB, int U, bool HOP, bool BATCH, bool PAD = false>
 __global__ void __launch_bounds__(kThreads, reduce_blocks_per_sm(WCAP, U, BATCH, reduce_wide_heads(WCAP, ALGO)))
 reduce_kernel(const __grid_constant__ ReduceParams P) {
     using A = Arith<DT, OP>;
@@ -683,12 +683,14 @@ reduce_kernel(const __grid_constant__ ReduceParams P) {
     // vectors are live at a time).
     constexpr bool kTable = BATCH;
     constexpr bool kTreeBatched = BATCH && ALGO == MR_TREE;
-    // The int32 trees over 16 slots fold the identity-padded tree (no
-    // condition on W inside a batch): at 9-11 ranks the conditional fold's
-    // branches (3x the ring's, ncu) held them at 5.67-5.84 TB/s; padded they
-    // run at 5.89-6.35 (sum 6.22-6.35).  The float trees measured slower
-    // padded (fp32 at 9-13 ranks 4-10 %) and keep the conditional fold.
-    constexpr bool kPaddedTree = kTreeBatched && DT == MR_INT32 && WCAP == 16;
+    // PAD: the identity-padded tree (no condition on W inside a batch), which
+    // the host takes for the int32 trees over 16 slots when W is not a
+    // multiple of 8: at 9-11 ranks the conditional fold's branches on the
+    // ragged last batch (3x the ring's, ncu) held them at 5.67-5.84 TB/s;
+    // padded they run at 5.89-6.35 (sum 6.21-6.35).  With whole batches
+    // (W = 16) the conditional fold measured 1-2.6 % faster, and the float
+    // trees 4-10 % slower padded at 9-13 ranks.
+    constexpr bool kPaddedTree = kTreeBatched && PAD;
     // The 32- and 64-slot trees keep their batches' top subtotals in dynamic
     // shared memory (see reduce_top_shared).
     constexpr bool kTopShared = kTreeBatched && WCAP >= 32;   // reduce_top_shared()
@@ -950,6 +952,10 @@ cudaError_t launch_reduce(const ReduceParams& P, int op, dim3 grid, cudaStream_t
                 if (rs) return launch_spread(reduce_kernel<DT, OP, ALGO, 8, 16, reduce_unroll_for(8, true), HOP, false>, grid, 0, stream, P);
                 return launch_spread(reduce_kernel<DT, OP, ALGO, 8, 16, reduce_unroll_for(8, false), HOP, false>, grid, 0, stream, P);
             case 16:
+                if constexpr (DT == MR_INT32 && ALGO == MR_TREE) {
+                    if (P.W % 8 != 0)
+                        return launch_spread(reduce_kernel<DT, OP, ALGO, 16, 16, 1, HOP, true, true>, grid, 0, stream, P);
+                }
                 if (reduce_batched(P.W, ALGO, DT, HOP))
                     return launch_spread(reduce_kernel<DT, OP, ALGO, 16, 16, 1, HOP, true>, grid, 0, stream, P);
                 return launch_spread(reduce_kernel<DT, OP, ALGO, 16, 16, reduce_unroll_for(16, false), HOP, false>, grid, 0, stream, P);

@@ -5,9 +5,9 @@ From 13 ranks up the CUDA kernel does not hold all W contributions of an
 element at once.  It loads the positions in batches [8m, 8m+8), folds each
 batch up to the node that the batch head's upper-child search finds inside it,
 and then folds the batch heads 8m as the same bit-trick tree one level up.
-The int32 trees over 16 slots run a second schedule: the positions past W
-padded with the op's exact identity and the whole tree folded with no
-condition on W.  This test restates both schedules on symbols and checks,
+The int32 trees over 16 slots run a second schedule when W is not a
+multiple of 8: the positions past W padded with the op's exact identity and
+the whole tree folded with no condition on W.  This test restates both schedules on symbols and checks,
 for every W from 9 to 64, that they perform the oracle's combines in the
 oracle's order (the padded one once its identities drop): each node's
 own value first, then its children's subtotals in the order the oracle lists
