@@ -90,12 +90,14 @@ template <int DT, int OP> struct Arith {
         }
     }
 
-    // The op's identity element e, exact in both orders (combine(a, e) and
-    // combine(e, a) are a, bit for bit, for every value a the folds carry,
-    // NaN and signed zeros included): -0.0 for float sums (x + -0.0 = x under
-    // round-to-nearest, and -0.0 + -0.0 = -0.0), 1 for products, the extreme
-    // keys for min and max, 0 for integer sums.  The batched tree pads the
-    // positions past W with it.
+    // The op's identity element e: combine(a, e) and combine(e, a) give a,
+    // bit for bit, for every integer a, and for every float a but a NaN,
+    // whose payload a GPU add or multiply may make canonical (min and max,
+    // folded on keys, keep even that): 0 or 1 for integer sums and products,
+    // the extreme value or key for min and max, -0.0 for float sums (x + -0.0
+    // = x under round-to-nearest, and -0.0 + -0.0 = -0.0), 1.0 for float
+    // products.  The identity-padded tree, which relies on it, runs for int32
+    // only.
     static __device__ __forceinline__ acc_t identity() {
         if constexpr (DT == MR_INT32) {
             if constexpr (OP == MR_SUM || OP == MR_AVG) return 0u;
